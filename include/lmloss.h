@@ -1,0 +1,189 @@
+/*
+ * lmloss: fused LM-head loss forward + backward over a [T, V] logit matrix,
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * One call computes, sharing one softmax pass per row:
+ *   - cross-entropy in the collapse-free form NLL = softplus(lse_{j!=t} z_j - z_t)
+ *       [torchtitan PR 5661 "fix softmax collapse with improved CE perf",
+ *        commit message, "Numerics (TP > 1 only)"];
+ *   - z-loss alpha * lse^2
+ *       [xtuner PR 1963 "[FSDP][Loss] Switch gradient reduction to SUM", z-loss diff];
+ *   - optional forward-KL distillation against teacher logits, and
+ *   - optional GSPO sequence-level clipped aggregation over packed segments
+ *       [Fast-LLM PR 552 "Fuse GSPO into the monolithic compiled loss (#507)",
+ *        "Why it needed special handling" and "Approach"],
+ * reduced either as a token mean or as a SUM over the caller's global
+ * denominator [xtuner PR 1963, description], and writes the gradient
+ * d(total)/d(logits) once, optionally over the logits in place.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE memory owned by the caller, row-major.
+ *     The library never frees or retains them past the call.
+ *   - Calls are asynchronous on the given stream; no entry point synchronises
+ *     the device except lmloss_get_device_error and lmloss_get_timing.
+ *   - Argument errors are detected on the host and returned synchronously
+ *     before anything is launched.  Data errors found on the device (a target
+ *     outside [0, V) that is not -100, a segment id >= num_segments, a GSPO
+ *     log-ratio sum out of range, a bounded wait that expired) are recorded in
+ *     the handle's device error word; the affected rows' losses and gradients
+ *     are NaN.  Read the word with lmloss_get_device_error after syncing.
+ *   - One handle per stream: two calls on one handle must not overlap.
+ */
+#ifndef LMLOSS_H
+#define LMLOSS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LMLOSS_OK = 0,
+    LMLOSS_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, ld < V, ...        */
+    LMLOSS_ERR_UNSUPPORTED = 2,   /* valid but not implemented (see lmloss_forward_backward) */
+    LMLOSS_ERR_CUDA = 3,          /* a CUDA runtime call failed                            */
+    LMLOSS_ERR_BAD_TARGET = 4,    /* device: target not in [0, V) and not -100             */
+    LMLOSS_ERR_BAD_SEGMENT = 5,   /* device: segment id >= num_segments                    */
+    LMLOSS_ERR_RANGE = 6,         /* device: GSPO log-ratio sum beyond +-2^31              */
+    LMLOSS_ERR_TIMEOUT = 7        /* device: a bounded wait on a copy expired              */
+} lmloss_status;
+
+typedef enum { LMLOSS_BF16 = 0, LMLOSS_FP32 = 1 } lmloss_dtype;
+
+typedef enum {
+    LMLOSS_REDUCE_SUM = 0,        /* every term scaled by 1 / denominator                  */
+    LMLOSS_REDUCE_TOKEN_MEAN = 1  /* token terms / #active tokens, GSPO / #non-empty segs   */
+} lmloss_reduction;
+
+#define LMLOSS_IGNORE_INDEX (-100)
+
+typedef struct lmloss_ctx* lmloss_handle;
+
+/*
+ * Arguments of one call.  Zero-initialise, then fill what is used.
+ *
+ * Layout: logits, teacher_logits and grad_out are [T, ld] row-major arrays of
+ * `dtype` (bf16 or fp32) whose first V columns are used; all three share ld.
+ * Elements must be naturally aligned, and teacher_logits / grad_out must sit at
+ * the same address modulo 16 bytes as logits (true for any two buffers from
+ * one allocator with the same ld).
+ *
+ * Row r is ACTIVE iff targets[r] != -100 and (loss_mask == NULL or
+ * loss_mask[r] != 0).  Inactive rows add nothing and get an all-zero gradient
+ * [torchtitan PR 5661, "Numerics": ignored labels are zeroed by the mask].
+ */
+typedef struct {
+    const void* logits;          /* [T, ld] dtype                                          */
+    int64_t T;                   /* rows (tokens), >= 0                                    */
+    int64_t V;                   /* vocabulary columns, >= 1                               */
+    int64_t ld;                  /* row stride in elements, >= V                           */
+    int32_t dtype;               /* lmloss_dtype                                           */
+    int32_t reduction;           /* lmloss_reduction                                       */
+    const int64_t* targets;      /* [T] target column, or -100 to ignore the row           */
+    const uint8_t* loss_mask;    /* [T] or NULL                                            */
+
+    float ce_weight;             /* weight of the CE term (0 for pure GSPO)                */
+    float z_alpha;               /* z-loss alpha; 0 disables                               */
+
+    const void* teacher_logits;  /* [T, ld] dtype, or NULL to disable distillation         */
+    float kl_weight;             /* weight of KL(softmax(teacher) || softmax(logits))      */
+    float temperature;           /* distillation temperature; only 1 is supported          */
+
+    const int32_t* segment_ids;  /* [T] GSPO segment of each row, -1 = none; NULL disables */
+    int32_t num_segments;        /* segments in this call, <= the handle's max_segments    */
+    const float* advantages;     /* [num_segments] per-segment advantage A_i               */
+    const float* old_logprobs;   /* [T] behaviour-policy log-prob of each target           */
+    float clip_eps_low;          /* ratio clipped to [1 - clip_eps_low, 1 + clip_eps_high] */
+    float clip_eps_high;
+
+    double denominator;          /* SUM reduction: every term is divided by this (> 0)     */
+
+    void* grad_out;              /* [T, ld] dtype; == logits writes in place; NULL = none  */
+    float* loss_out;             /* [5] total, ce, z, kl, gspo (each after its scale)      */
+    float* logp_out;             /* optional [T]: log p_target = -NLL (0 on inactive rows) */
+    float* lse_out;              /* optional [T]: logsumexp of the row (0 on inactive)     */
+    float* kl_out;               /* optional [T]: per-row KL (0 on inactive / no teacher)  */
+    int64_t* count_out;          /* optional [2]: active rows, non-empty GSPO segments     */
+    int32_t* seg_count_out;      /* optional [num_segments]: active tokens per segment     */
+    float* seg_ratio_out;        /* optional [num_segments]: s_i = exp(mean log-ratio)     */
+    uint8_t* seg_flag_out;       /* optional [num_segments]: 1 iff gradient flows via s_i  */
+    float* seg_loss_out;         /* optional [num_segments]: L_i before the GSPO scale     */
+} lmloss_args;
+
+/* What the last call launched (for tuning and for benchmark bookkeeping). */
+typedef struct {
+    int32_t launches;            /* kernels launched by the call                           */
+    int32_t path;                /* 0 fused single-read, 1 stats-only, 2 GSPO three-phase  */
+    int32_t cluster;             /* CTAs per row in the fused kernel                       */
+    int32_t threads;             /* threads per CTA of the main kernel                     */
+    int32_t nbuf;                /* staged rows per CTA in the fused kernel                */
+    int32_t grid;                /* CTAs of the main kernel                                */
+    int32_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel       */
+    int32_t reserved;
+} lmloss_call_info;
+
+/* Create a handle on `device`: allocates the workspace for calls with up to
+ * max_T rows and max_segments GSPO segments (about 12 B per row plus 40 B per
+ * segment) and the device error word.  The caller owns the handle. */
+lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, int32_t max_segments);
+
+/* Free the handle and its workspace.  Synchronises the handle's device. */
+lmloss_status lmloss_destroy(lmloss_handle handle);
+
+/* Host-only validation of `args` (no CUDA call).  Returns what
+ * lmloss_forward_backward would return before launching anything, except
+ * for the handle's capacity limits. */
+lmloss_status lmloss_check_args(const lmloss_args* args);
+
+/*
+ * Loss and gradient for one batch, asynchronous on `stream`.
+ *
+ * Paths:
+ *   - no GSPO, grad_out != NULL: one fused kernel reads every active row once
+ *     (staged in shared memory across a thread-block cluster), reduces its
+ *     max / non-target sum / teacher statistics through distributed shared
+ *     memory, and writes the gradient once;
+ *   - no GSPO, grad_out == NULL: forward statistics only;
+ *   - GSPO: statistics pass, segment seam, gradient pass (the seam must see
+ *     every row of a segment before any gradient, so the logits are read twice)
+ *     [Fast-LLM PR 552, "Approach": GSPO's backward follows its eager seam].
+ * Unsupported (LMLOSS_ERR_UNSUPPORTED): temperature != 1 with a teacher;
+ * teacher together with GSPO.
+ * loss_out is written on every path.  The gradient is
+ *   s * (ce_weight (p - onehot) + 2 z_alpha lse p + kl_weight (p - q)) + c_r (p - onehot)
+ * with s the token scale and c_r the row's GSPO coefficient; it is rounded to
+ * nearest-even into dtype.
+ */
+lmloss_status lmloss_forward_backward(lmloss_handle handle, const lmloss_args* args, cudaStream_t stream);
+
+/* Read and clear the device error word.  Synchronises the handle's device.
+ * Returns LMLOSS_OK when no device-side data error occurred since the last read. */
+lmloss_status lmloss_get_device_error(lmloss_handle handle);
+
+/* Human-readable name of a status. */
+const char* lmloss_status_string(lmloss_status status);
+
+/* Override the fused kernel's launch shape: cluster size (1..16), threads per
+ * CTA (128, 256, 384, 512 or 1024) and rows staged per CTA (1 or 2).  0 keeps
+ * the automatic choice.  Shapes that do not fit are rejected at the next call
+ * with LMLOSS_ERR_UNSUPPORTED. */
+lmloss_status lmloss_set_launch_config(lmloss_handle handle, int cluster, int threads, int nbuf);
+
+/* When enabled (which also resets the record), each call records a pair of
+ * CUDA events on its stream around its main kernel(s), up to 4096 calls.
+ * lmloss_get_timing waits for the last pair and returns the summed elapsed
+ * time of every recorded call and how many calls were recorded. */
+lmloss_status lmloss_set_timing(lmloss_handle handle, int enable);
+lmloss_status lmloss_get_timing(lmloss_handle handle, float* total_ms, int32_t* calls);
+
+/* Launch shape and kernel count of the last call on this handle. */
+lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMLOSS_H */

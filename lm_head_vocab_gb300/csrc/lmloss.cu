@@ -1,0 +1,492 @@
+// Host side of the lmloss C ABI: argument validation, workspace, launch
+// planning and kernel sequencing.  Every step of the loss runs in the kernels
+// of kernels.cuh; nothing here touches tensor data.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "../../include/lmloss.h"
+#include "kernels.cuh"
+
+using namespace lmloss;
+
+struct lmloss_ctx {
+    int device = 0;
+    int64_t max_T = 0;
+    int32_t max_S = 0;
+    void* ws_mem = nullptr;
+    Workspace ws{};
+    int cfg_cluster = 0, cfg_threads = 0, cfg_nbuf = 0;
+    int timing = 0;
+    static constexpr int kMaxTimed = 4096;
+    cudaEvent_t* ev = nullptr;   // [2 * kMaxTimed], created on first use
+    int ev_created = 0;          // pairs created
+    int ev_used = 0;             // pairs recorded since timing was enabled
+    lmloss_call_info info{};
+    int num_sms = 0;
+    int smem_optin = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool misaligned(const void* a, const void* b)
+{
+    return ((reinterpret_cast<uintptr_t>(a) - reinterpret_cast<uintptr_t>(b)) & 15u) != 0;
+}
+
+lmloss_status check(const lmloss_args* a)
+{
+    if (!a) return LMLOSS_ERR_INVALID_ARG;
+    if (a->T < 0 || a->V < 1 || a->ld < a->V) return LMLOSS_ERR_INVALID_ARG;
+    if (a->dtype != LMLOSS_BF16 && a->dtype != LMLOSS_FP32) return LMLOSS_ERR_INVALID_ARG;
+    if (a->reduction != LMLOSS_REDUCE_SUM && a->reduction != LMLOSS_REDUCE_TOKEN_MEAN) return LMLOSS_ERR_INVALID_ARG;
+    if (!a->loss_out) return LMLOSS_ERR_INVALID_ARG;
+    const int esz = a->dtype == LMLOSS_BF16 ? 2 : 4;
+    if (a->T > 0) {
+        if (!a->logits || !a->targets) return LMLOSS_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(a->logits) % esz) return LMLOSS_ERR_INVALID_ARG;
+        // T * ld elements must be addressable in bytes with int64
+        if (a->ld > (INT64_MAX / 8) / a->T) return LMLOSS_ERR_INVALID_ARG;
+    }
+    if (a->reduction == LMLOSS_REDUCE_SUM && !(a->denominator > 0.0 && std::isfinite(a->denominator)))
+        return LMLOSS_ERR_INVALID_ARG;
+    if (!std::isfinite(a->ce_weight) || !std::isfinite(a->z_alpha)) return LMLOSS_ERR_INVALID_ARG;
+    if (a->grad_out && a->T > 0 && misaligned(a->grad_out, a->logits)) return LMLOSS_ERR_INVALID_ARG;
+    if (a->teacher_logits) {
+        if (a->T > 0 && misaligned(a->teacher_logits, a->logits)) return LMLOSS_ERR_INVALID_ARG;
+        if (!std::isfinite(a->kl_weight) || !(a->temperature > 0.f)) return LMLOSS_ERR_INVALID_ARG;
+        if (a->temperature != 1.0f) return LMLOSS_ERR_UNSUPPORTED;
+        if (a->grad_out == a->teacher_logits) return LMLOSS_ERR_INVALID_ARG;
+    }
+    if (a->segment_ids) {
+        if (a->num_segments < 0) return LMLOSS_ERR_INVALID_ARG;
+        if (a->T > 0 && !a->old_logprobs) return LMLOSS_ERR_INVALID_ARG;
+        if (a->num_segments > 0 && !a->advantages) return LMLOSS_ERR_INVALID_ARG;
+        if (!(a->clip_eps_low >= 0.f) || !(a->clip_eps_high >= 0.f)) return LMLOSS_ERR_INVALID_ARG;
+        if (a->teacher_logits) return LMLOSS_ERR_UNSUPPORTED;
+    }
+    return LMLOSS_OK;
+}
+
+// ------------------------------------------------------------ launch plans
+template <bool BF16, bool KL, int NT>
+const void* fused_ptr() { return reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT>); }
+
+const void* pick_fused(bool bf16, bool kl, int nt)
+{
+#define LMLOSS_PICK(NTV)                                                            \
+    if (nt == NTV) {                                                                \
+        if (bf16) return kl ? fused_ptr<true, true, NTV>() : fused_ptr<true, false, NTV>(); \
+        return kl ? fused_ptr<false, true, NTV>() : fused_ptr<false, false, NTV>();  \
+    }
+    LMLOSS_PICK(128)
+    LMLOSS_PICK(256)
+    LMLOSS_PICK(512)
+    LMLOSS_PICK(1024)
+#undef LMLOSS_PICK
+    return nullptr;
+}
+
+struct FusedPlan {
+    const void* fn = nullptr;
+    int C = 0, NT = 0, nbuf = 0, grid = 0;
+    int64_t slice = 0;
+    uint32_t buf_bytes = 0;
+    size_t smem = 0;
+};
+
+size_t fused_smem(int64_t V, int C, int nbuf, bool kl, int esz, int64_t* slice_out, uint32_t* buf_out)
+{
+    const int vn = 16 / esz;
+    int64_t slice = (V + C - 1) / C;
+    slice = (slice + vn - 1) / vn * vn;
+    const uint32_t buf = static_cast<uint32_t>(align_up(static_cast<size_t>(slice) * esz, 128));
+    if (slice_out) *slice_out = slice;
+    if (buf_out) *buf_out = buf;
+    return kHdrBytes + static_cast<size_t>(nbuf) * (kl ? 2 : 1) * buf;
+}
+
+lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
+{
+    const bool bf16 = a->dtype == LMLOSS_BF16;
+    const bool kl = a->teacher_logits != nullptr;
+    const int esz = bf16 ? 2 : 4;
+    int NT = h->cfg_threads ? h->cfg_threads : (bf16 ? 512 : 256);
+    int nbuf = h->cfg_nbuf ? h->cfg_nbuf : 2;
+    int C = h->cfg_cluster;
+    if (!C) {
+        // smallest cluster whose staged slices leave room for two CTAs per SM,
+        // else the smallest that fits at all
+        const size_t half = static_cast<size_t>(h->smem_optin) / 2 - 1024;
+        for (int c = 1; c <= 16 && !C; ++c)
+            if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= half) C = c;
+        for (int c = 1; c <= 16 && !C; ++c)
+            if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= static_cast<size_t>(h->smem_optin)) C = c;
+        if (!C && !h->cfg_nbuf) {
+            nbuf = 1;
+            for (int c = 1; c <= 16 && !C; ++c)
+                if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= static_cast<size_t>(h->smem_optin)) C = c;
+        }
+        if (!C) return LMLOSS_ERR_UNSUPPORTED;
+    }
+    if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
+    P.fn = pick_fused(bf16, kl, NT);
+    if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
+    P.C = C;
+    P.NT = NT;
+    P.nbuf = nbuf;
+    P.smem = fused_smem(a->V, C, nbuf, kl, esz, &P.slice, &P.buf_bytes);
+    if (P.smem > static_cast<size_t>(h->smem_optin)) return LMLOSS_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(P.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P.smem)) != cudaSuccess)
+        return LMLOSS_ERR_CUDA;
+    if (C > 8 && cudaFuncSetAttribute(P.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return LMLOSS_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(C * h->num_sms));
+    cfg.blockDim = dim3(static_cast<unsigned>(NT));
+    cfg.dynamicSmemBytes = P.smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, P.fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return LMLOSS_ERR_UNSUPPORTED;
+    }
+    if (nclusters < 1) return LMLOSS_ERR_UNSUPPORTED;
+    int64_t want = a->T < nclusters ? a->T : nclusters;
+    if (want < 1) want = 1;
+    P.grid = static_cast<int>(want) * C;
+    return LMLOSS_OK;
+}
+
+template <typename K>
+int resident_grid(K kernel, int threads, int num_sms, int64_t rows)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    int64_t g = static_cast<int64_t>(per_sm) * num_sms;
+    if (rows < g) g = rows;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+lmloss_status launch_err()
+{
+    return cudaGetLastError() == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lmloss_status_string(lmloss_status s)
+{
+    switch (s) {
+    case LMLOSS_OK: return "ok";
+    case LMLOSS_ERR_INVALID_ARG: return "invalid argument";
+    case LMLOSS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LMLOSS_ERR_CUDA: return "CUDA runtime error";
+    case LMLOSS_ERR_BAD_TARGET: return "target outside [0, V) and not ignore_index";
+    case LMLOSS_ERR_BAD_SEGMENT: return "segment id outside [0, num_segments)";
+    case LMLOSS_ERR_RANGE: return "GSPO log-ratio sum out of range";
+    case LMLOSS_ERR_TIMEOUT: return "bounded wait on a copy expired";
+    }
+    return "unknown status";
+}
+
+lmloss_status lmloss_check_args(const lmloss_args* args) { return check(args); }
+
+lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, int32_t max_segments)
+{
+    if (!handle || max_T < 0 || max_segments < 0) return LMLOSS_ERR_INVALID_ARG;
+    *handle = nullptr;
+    DeviceGuard g(device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    lmloss_ctx* h = new (std::nothrow) lmloss_ctx();
+    if (!h) return LMLOSS_ERR_CUDA;
+    h->device = device;
+    h->max_T = max_T;
+    h->max_S = max_segments;
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+        delete h;
+        return LMLOSS_ERR_CUDA;
+    }
+    const size_t T = static_cast<size_t>(max_T > 0 ? max_T : 1);
+    const size_t S = static_cast<size_t>(max_segments > 0 ? max_segments : 1);
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_nll = take(4 * T), o_lse = take(4 * T), o_kl = take(4 * T);
+    const size_t o_scal = take(64);
+    const size_t o_sn = take(4 * S), o_dq = take(8 * S), o_aq = take(8 * S), o_nf = take(12 * S), o_coef = take(4 * S);
+    const size_t o_err = take(16);
+    if (cudaMalloc(&h->ws_mem, off) != cudaSuccess) {
+        delete h;
+        return LMLOSS_ERR_CUDA;
+    }
+    char* base = static_cast<char*>(h->ws_mem);
+    h->ws.row_nll = reinterpret_cast<float*>(base + o_nll);
+    h->ws.row_lse = reinterpret_cast<float*>(base + o_lse);
+    h->ws.row_kl = reinterpret_cast<float*>(base + o_kl);
+    h->ws.n_active = reinterpret_cast<int64_t*>(base + o_scal);
+    h->ws.n_nonempty = reinterpret_cast<int64_t*>(base + o_scal + 8);
+    h->ws.gspo_sum = reinterpret_cast<double*>(base + o_scal + 16);
+    h->ws.s_seg = reinterpret_cast<double*>(base + o_scal + 24);
+    h->ws.seg_n = reinterpret_cast<int*>(base + o_sn);
+    h->ws.seg_dq = reinterpret_cast<unsigned long long*>(base + o_dq);
+    h->ws.seg_absq = reinterpret_cast<unsigned long long*>(base + o_aq);
+    h->ws.seg_nonfinite = reinterpret_cast<int*>(base + o_nf);
+    h->ws.seg_coef = reinterpret_cast<float*>(base + o_coef);
+    h->ws.err = reinterpret_cast<int*>(base + o_err);
+    h->ev = static_cast<cudaEvent_t*>(std::calloc(2 * lmloss_ctx::kMaxTimed, sizeof(cudaEvent_t)));
+    if (!h->ev || cudaMemset(h->ws_mem, 0, off) != cudaSuccess) {
+        std::free(h->ev);
+        cudaFree(h->ws_mem);
+        delete h;
+        return LMLOSS_ERR_CUDA;
+    }
+    *handle = h;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_destroy(lmloss_handle h)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    for (int i = 0; i < 2 * h->ev_created; ++i) cudaEventDestroy(h->ev[i]);
+    std::free(h->ev);
+    cudaError_t e = cudaFree(h->ws_mem);
+    delete h;
+    return e == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
+}
+
+lmloss_status lmloss_set_launch_config(lmloss_handle h, int cluster, int threads, int nbuf)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    if (cluster < 0 || cluster > 16) return LMLOSS_ERR_INVALID_ARG;
+    if (threads != 0 && threads != 128 && threads != 256 && threads != 512 && threads != 1024)
+        return LMLOSS_ERR_INVALID_ARG;
+    if (nbuf < 0 || nbuf > 2) return LMLOSS_ERR_INVALID_ARG;
+    h->cfg_cluster = cluster;
+    h->cfg_threads = threads;
+    h->cfg_nbuf = nbuf;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_set_timing(lmloss_handle h, int enable)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    h->timing = enable ? 1 : 0;
+    h->ev_used = 0;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_get_timing(lmloss_handle h, float* total_ms, int32_t* calls)
+{
+    if (!h || !total_ms) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    float sum = 0.f;
+    for (int i = 0; i < h->ev_used; ++i) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(h->ev[2 * i + 1]) != cudaSuccess) return LMLOSS_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms, h->ev[2 * i], h->ev[2 * i + 1]) != cudaSuccess) return LMLOSS_ERR_CUDA;
+        sum += ms;
+    }
+    *total_ms = sum;
+    if (calls) *calls = h->ev_used;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_get_call_info(lmloss_handle h, lmloss_call_info* info)
+{
+    if (!h || !info) return LMLOSS_ERR_INVALID_ARG;
+    *info = h->info;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_get_device_error(lmloss_handle h)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok || cudaDeviceSynchronize() != cudaSuccess) return LMLOSS_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, h->ws.err, sizeof code, cudaMemcpyDeviceToHost) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    if (cudaMemset(h->ws.err, 0, sizeof code) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    return static_cast<lmloss_status>(code);
+}
+
+lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cudaStream_t stream)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    lmloss_status st = check(a);
+    if (st != LMLOSS_OK) return st;
+    if (a->T > h->max_T) return LMLOSS_ERR_INVALID_ARG;
+    if (a->segment_ids && a->num_segments > h->max_S) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+
+    const bool bf16 = a->dtype == LMLOSS_BF16;
+    const bool kl = a->teacher_logits != nullptr;
+    const bool gspo = a->segment_ids != nullptr;
+
+    CallParams p{};
+    p.logits = a->logits;
+    p.teacher = a->teacher_logits;
+    p.grad = a->grad_out;
+    p.targets = a->targets;
+    p.mask = a->loss_mask;
+    p.T = a->T;
+    p.V = a->V;
+    p.ld = a->ld;
+    p.w_ce = a->ce_weight;
+    p.alpha = a->z_alpha;
+    p.w_kl = kl ? a->kl_weight : 0.f;
+    p.reduction = a->reduction;
+    p.inv_denominator = a->reduction == LMLOSS_REDUCE_SUM ? 1.0 / a->denominator : 0.0;
+    p.seg_ids = a->segment_ids;
+    p.num_segments = gspo ? a->num_segments : 0;
+    p.adv = a->advantages;
+    p.old_logp = a->old_logprobs;
+    p.eps_lo = a->clip_eps_low;
+    p.eps_hi = a->clip_eps_high;
+    p.loss_out = a->loss_out;
+    p.logp_out = a->logp_out;
+    p.lse_out = a->lse_out;
+    p.kl_out = a->kl_out;
+    p.count_out = a->count_out;
+    p.seg_count_out = a->seg_count_out;
+    p.seg_ratio_out = a->seg_ratio_out;
+    p.seg_flag_out = a->seg_flag_out;
+    p.seg_loss_out = a->seg_loss_out;
+    p.ws = h->ws;
+
+    lmloss_call_info info{};
+    const int NT_STREAM = 512;
+
+    count_kernel<<<1, 1024, 0, stream>>>(p);
+    if ((st = launch_err()) != LMLOSS_OK) return st;
+    info.launches = 1;
+
+    int ev_slot = -1;
+    if (h->timing && h->ev_used < lmloss_ctx::kMaxTimed) {
+        ev_slot = h->ev_used;
+        if (ev_slot >= h->ev_created) {
+            if (cudaEventCreate(&h->ev[2 * ev_slot]) != cudaSuccess ||
+                cudaEventCreate(&h->ev[2 * ev_slot + 1]) != cudaSuccess)
+                return LMLOSS_ERR_CUDA;
+            h->ev_created = ev_slot + 1;
+        }
+        cudaEventRecord(h->ev[2 * ev_slot], stream);
+    }
+    if (a->T > 0) {
+        if (!gspo && a->grad_out) {
+            FusedPlan P;
+            if ((st = plan_fused(h, a, P)) != LMLOSS_OK) return st;
+            p.cluster = P.C;
+            p.slice = P.slice;
+            p.nbuf = P.nbuf;
+            p.buf_bytes = P.buf_bytes;
+            cudaLaunchConfig_t cfg{};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = P.C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(P.grid));
+            cfg.blockDim = dim3(static_cast<unsigned>(P.NT));
+            cfg.dynamicSmemBytes = P.smem;
+            cfg.stream = stream;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            void* kargs[] = {&p};
+            if (cudaLaunchKernelExC(&cfg, P.fn, kargs) != cudaSuccess) {
+                cudaGetLastError();
+                return LMLOSS_ERR_CUDA;
+            }
+            info.launches += 1;
+            info.path = 0;
+            info.cluster = P.C;
+            info.threads = P.NT;
+            info.nbuf = P.nbuf;
+            info.grid = P.grid;
+            info.smem_bytes = static_cast<int32_t>(P.smem);
+        } else {
+            int grid;
+            if (bf16) {
+                if (kl) { grid = resident_grid(stats_kernel<true, true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                          stats_kernel<true, true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
+                else    { grid = resident_grid(stats_kernel<true, false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                          stats_kernel<true, false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
+            } else {
+                if (kl) { grid = resident_grid(stats_kernel<false, true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                          stats_kernel<false, true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
+                else    { grid = resident_grid(stats_kernel<false, false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                          stats_kernel<false, false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
+            }
+            if ((st = launch_err()) != LMLOSS_OK) return st;
+            info.launches += 1;
+            info.path = gspo ? 2 : 1;
+            info.cluster = 1;
+            info.threads = NT_STREAM;
+            info.grid = grid;
+            if (gspo) {
+                const int tg = 256;
+                int64_t gb = (a->T + tg - 1) / tg;
+                if (gb > 4LL * h->num_sms) gb = 4LL * h->num_sms;
+                seam_accum_kernel<<<static_cast<unsigned>(gb), tg, 0, stream>>>(p);
+                if ((st = launch_err()) != LMLOSS_OK) return st;
+                seam_finish_kernel<<<1, 1024, 0, stream>>>(p);
+                if ((st = launch_err()) != LMLOSS_OK) return st;
+                info.launches += 2;
+                if (a->grad_out) {
+                    if (bf16) {
+                        grid = resident_grid(grad_kernel<true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                        grad_kernel<true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p);
+                    } else {
+                        grid = resident_grid(grad_kernel<false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
+                        grad_kernel<false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p);
+                    }
+                    if ((st = launch_err()) != LMLOSS_OK) return st;
+                    info.launches += 1;
+                }
+            }
+        }
+    }
+    if (ev_slot >= 0) {
+        cudaEventRecord(h->ev[2 * ev_slot + 1], stream);
+        h->ev_used = ev_slot + 1;
+    }
+    reduce_kernel<<<1, 1024, 0, stream>>>(p);
+    if ((st = launch_err()) != LMLOSS_OK) return st;
+    info.launches += 1;
+    h->info = info;
+    return LMLOSS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+"""Helpers for the GPU parity tests: move seeded host inputs to the device, run
+the CUDA path through the C ABI, and compare with the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+BF16_TINY = 2.0 ** -126
+
+
+def to_device(x: np.ndarray, dev) -> torch.Tensor:
+    if x.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+
+def grad_to_f64(g: torch.Tensor) -> np.ndarray:
+    return g.float().cpu().numpy().astype(np.float64)
+
+
+def bf16_ulp(ref: np.ndarray) -> np.ndarray:
+    """One bf16 ulp at |ref| (8 significant bits); floor at the smallest normal."""
+    a = np.maximum(np.abs(ref), BF16_TINY)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bf16: bool, what: str = ""):
+    """bf16: within 1 ulp of the fp64 value (values below 2^-126 may flush to 0);
+    fp32: within 1e-6 absolute.  Exact zeros (inactive rows) must stay exact."""
+    assert g_gpu.shape == g_ref.shape
+    assert np.all(np.isfinite(g_gpu)), f"{what}: non-finite gradient"
+    zero = g_ref == 0.0
+    assert np.all(g_gpu[zero] == 0.0), f"{what}: nonzero gradient where the oracle has exact 0"
+    err = np.abs(g_gpu - g_ref)
+    if bf16:
+        tiny = np.abs(g_ref) < BF16_TINY
+        ok = (err <= bf16_ulp(g_ref)) | (tiny & (np.abs(g_gpu) <= BF16_TINY))
+        worst = float(np.max(np.where(tiny, 0.0, err / bf16_ulp(g_ref)))) if g_ref.size else 0.0
+        assert ok.all(), f"{what}: {int((~ok).sum())} elements beyond 1 bf16 ulp (worst {worst:.3f} ulp)"
+        return worst
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= 1e-6, f"{what}: max abs error {worst:.3e} > 1e-6"
+    return worst
+
+
+def rel(a, b):
+    return abs(a - b) / max(abs(b), 1e-300)
+
+
+class Case:
+    """A workload instance: host arrays, the oracle problem and device tensors."""
+
+    def __init__(self, w: workloads.Workload, dev, rows: int = None):
+        self.w = w
+        self.dev = dev
+        self.targets = w.targets()
+        self.mask = w.loss_mask()
+        x = w.logits_rows(0, w.T)
+        self.x = x
+        self.u = w.teacher_rows(0, w.T, x)
+        self.seg, self.S, self.adv = w.segments()
+        self.old = None
+        self.P = oracle.Problem(
+            logits=x, V=w.V, targets=self.targets, loss_mask=self.mask, ce_weight=w.ce_weight,
+            z_alpha=w.z_alpha, teacher=self.u, kl_weight=w.kl_weight, temperature=w.temperature,
+            reduction=oracle.REDUCE_SUM if w.reduction == "sum_active" else oracle.REDUCE_TOKEN_MEAN,
+            denominator=w.denominator())
+        if w.has_gspo:
+            # old log-probs: the oracle's fp64 log-prob plus the seeded noise
+            R0 = oracle.forward(oracle.Problem(logits=x, V=w.V, targets=self.targets, loss_mask=self.mask))
+            self.old = (R0.logp + w.old_logp_noise()).astype(np.float32)
+            self.P.segment_ids = self.seg
+            self.P.num_segments = self.S
+            self.P.advantages = self.adv
+            self.P.old_logprobs = self.old
+            self.P.clip_eps_low = w.clip_eps_low
+            self.P.clip_eps_high = w.clip_eps_high
+
+    def device_inputs(self):
+        d = self.dev
+        inp = dict(logits=to_device(self.x, d), targets=torch.from_numpy(self.targets).to(d))
+        inp["loss_mask"] = None if self.mask is None else torch.from_numpy(self.mask).to(d)
+        inp["teacher_logits"] = None if self.u is None else to_device(self.u, d)
+        if self.w.has_gspo:
+            inp["segment_ids"] = torch.from_numpy(self.seg).to(d)
+            inp["advantages"] = torch.from_numpy(self.adv).to(d)
+            inp["old_logprobs"] = torch.from_numpy(self.old).to(d)
+        return inp
+
+    def kwargs(self):
+        w = self.w
+        kw = dict(ce_weight=w.ce_weight, z_alpha=w.z_alpha, kl_weight=w.kl_weight,
+                  temperature=w.temperature,
+                  reduction="sum" if w.reduction == "sum_active" else "token_mean",
+                  denominator=w.denominator())
+        if w.has_gspo:
+            kw.update(num_segments=self.S, clip_eps_low=w.clip_eps_low, clip_eps_high=w.clip_eps_high)
+        return kw

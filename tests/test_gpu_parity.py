@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.
+
+Tolerances (from the arithmetic, fixed here):
+  losses            relative 1e-5;
+  bf16 gradients    within 1 bf16 ulp of the fp64 value (a value below 2^-126
+                    may flush to 0);
+  fp32 gradients    absolute 1e-6;
+  integer outputs   bit-exact (active count, segment counts, segment flags
+                    away from a clip bound, masked rows exactly 0).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_util import Case, check_grad, grad_to_f64, rel, to_device
+
+pytestmark = pytest.mark.gpu
+
+WANT = ("logp", "lse", "kl", "count", "seg")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def handle(dev):
+    from lm_head_vocab_gb300 import LMLoss
+    h = LMLoss(0, max_T=1 << 17, max_segments=1 << 14)
+    yield h
+    h.close()
+
+
+def run(handle, case, grad="new", inp=None):
+    inp = inp or case.device_inputs()
+    kw = case.kwargs()
+    out = handle.forward_backward(
+        inp["logits"], inp["targets"], inp["loss_mask"], teacher_logits=inp["teacher_logits"],
+        segment_ids=inp.get("segment_ids"), advantages=inp.get("advantages"),
+        old_logprobs=inp.get("old_logprobs"), grad=grad, want=WANT, **kw)
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    return inp, out
+
+
+def compare_all(case, out, R, g_ref, what):
+    bf16 = case.w.dtype == "bf16"
+    loss = out.loss.cpu().numpy().astype(np.float64)
+    ref = [R.total, R.ce, R.z, R.kl_loss, R.gspo]
+    for k, name in enumerate(["total", "ce", "z", "kl", "gspo"]):
+        if ref[k] == 0.0:
+            assert abs(loss[k]) <= 1e-30, (what, name, loss[k])
+        else:
+            assert rel(loss[k], ref[k]) <= 1e-5, (what, name, loss[k], ref[k])
+    cnt = out.count.cpu().numpy()
+    assert cnt[0] == R.n_active
+    act = R.active.astype(bool)
+    logp = out.logp.cpu().numpy().astype(np.float64)
+    lse = out.lse.cpu().numpy().astype(np.float64)
+    assert np.all(logp[~act] == 0.0) and np.all(lse[~act] == 0.0)
+    # per-row diagnostics
+    np.testing.assert_allclose(lse[act], R.lse[act], rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(logp[act], R.logp[act], rtol=2e-5, atol=1e-6)
+    if out.kl is not None:
+        np.testing.assert_allclose(out.kl.cpu().numpy()[act], R.kl[act], rtol=1e-4, atol=2e-6)
+    if out.grad is not None:
+        check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what)
+
+
+SMALL = [
+    ("ce_fp32_small", None),
+    ("ce_z_bf16", dict(T=256, V=32000)),
+    ("ce_z_bf16", dict(T=97, V=32003)),            # rows not 16-byte aligned
+    ("ce_z_bf16", dict(T=64, V=32003, ld=32016)),  # ragged tail, padded stride
+    ("confident_bf16", dict(T=128, V=128256)),
+    ("gspo_z_bf16", dict(T=1024, V=151936, packed_len=256)),
+    ("ce_z_kl_bf16", dict(T=64, V=262144)),
+    ("ce_z_kl_bf16", dict(T=40, V=5001)),
+    ("ce_fp32_small", dict(T=33, V=1027)),          # fp32, unaligned rows
+]
+
+
+def _case(dev, name, shape):
+    w = workloads.get(name)
+    if shape:
+        w = w.with_shape(**shape)
+    return Case(w, dev)
+
+
+@pytest.mark.parametrize("name,shape", SMALL, ids=[f"{n}-{s}" for n, s in SMALL])
+def test_parity_small(dev, handle, name, shape):
+    case = _case(dev, name, shape)
+    R, g_ref = oracle.forward_backward(case.P)
+    inp, out = run(handle, case)
+    compare_all(case, out, R, g_ref, f"{name} {shape}")
+    if case.w.has_gspo:
+        sc = out.seg_count.cpu().numpy()
+        assert np.array_equal(sc, R.seam.n)
+        assert out.count.cpu().numpy()[1] == R.seam.nonempty
+        flag = out.seg_flag.cpu().numpy()
+        s = R.seam.ratio
+        lo, hi = 1 - case.w.clip_eps_low, 1 + case.w.clip_eps_high
+        amb = (np.abs(s - lo) < 1e-6 * lo) | (np.abs(s - hi) < 1e-6 * hi)
+        assert np.array_equal(flag[~amb], R.seam.flag[~amb])
+        np.testing.assert_allclose(out.seg_ratio.cpu().numpy()[R.seam.n > 0], s[R.seam.n > 0], rtol=1e-6)
+    # in place gives the same bits as out of place
+    logits2 = inp["logits"].clone()
+    inp2 = dict(inp, logits=logits2)
+    _, out2 = run(handle, case, grad="inplace", inp=inp2)
+    assert torch.equal(out2.grad.view(torch.int16) if out2.grad.dtype == torch.bfloat16 else out2.grad,
+                       out.grad.view(torch.int16) if out.grad.dtype == torch.bfloat16 else out.grad)
+    assert torch.equal(out2.loss, out.loss)
+
+
+def test_confident_rows_properties(dev, handle):
+    """Planted margins 15..40: NLL > 0, target gradient < 0, rows sum to ~0."""
+    case = _case(dev, "confident_bf16", dict(T=256, V=128256))
+    _, out = run(handle, case)
+    m = case.w.margins()
+    planted = np.where(np.isfinite(m))[0]
+    assert len(planted) > 50
+    logp = out.logp.cpu().numpy()
+    g = grad_to_f64(out.grad)
+    t = case.targets
+    for r in planted:
+        assert logp[r] < 0.0
+        assert g[r, t[r]] < 0.0
+        assert abs(g[r].sum()) <= 2.0 ** -8 * np.abs(g[r]).sum()
+
+
+def test_deterministic_repeat(dev, handle):
+    case = _case(dev, "ce_z_kl_bf16", dict(T=48, V=70000))
+    inp = case.device_inputs()
+    _, a = run(handle, case, inp=inp)
+    _, b = run(handle, case, inp=inp)
+    assert torch.equal(a.grad.view(torch.int16), b.grad.view(torch.int16))
+    assert torch.equal(a.loss, b.loss)
+
+
+@pytest.mark.parametrize("cluster,threads,nbuf", [(1, 256, 1), (2, 512, 2), (3, 512, 1), (4, 256, 2),
+                                                  (8, 512, 2), (16, 128, 1)])
+def test_launch_shapes(dev, handle, cluster, threads, nbuf):
+    case = _case(dev, "ce_z_bf16", dict(T=96, V=50021))
+    R, g_ref = oracle.forward_backward(case.P)
+    handle.set_launch_config(cluster, threads, nbuf)
+    try:
+        _, out = run(handle, case)
+        info = handle.call_info()
+        assert info["cluster"] == cluster and info["threads"] == threads and info["nbuf"] == nbuf
+        compare_all(case, out, R, g_ref, f"shape {cluster},{threads},{nbuf}")
+    finally:
+        handle.set_launch_config(0, 0, 0)
+
+
+def test_shard_sum_bitwise(dev, handle):
+    """Rows split into shards, each called with SUM over the global active count,
+    give the full token-mean call's gradient bit for bit, and losses that add up."""
+    case = _case(dev, "ce_z_bf16", dict(T=200, V=32000))
+    inp = case.device_inputs()
+    w = case.w
+    _, full = handle_run_mean(handle, case, inp)
+    N = float(case.P.denominator)   # workload reduction is SUM over the active count
+    parts = []
+    tot = 0.0
+    for lo, hi in [(0, 77), (77, 150), (150, 200)]:
+        out = handle.forward_backward(inp["logits"][lo:hi], inp["targets"][lo:hi], None, z_alpha=w.z_alpha,
+                                      reduction="sum", denominator=N, grad="new")
+        torch.cuda.synchronize()
+        parts.append(out.grad)
+        tot += float(out.loss[0])
+    assert torch.equal(torch.cat(parts).view(torch.int16), full.grad.view(torch.int16))
+    assert rel(tot, float(full.loss[0])) <= 1e-6
+
+
+def handle_run_mean(handle, case, inp):
+    out = handle.forward_backward(inp["logits"], inp["targets"], None, z_alpha=case.w.z_alpha,
+                                  reduction="token_mean", grad="new")
+    torch.cuda.synchronize()
+    return inp, out
+
+
+# ------------------------------------------------------------------- edges
+def _tiny_problem(dev, handle, z, t, dtype, mask=None, **kw):
+    x = z.astype(np.float32)
+    host = workloads.bf16_round(x) if dtype == "bf16" else x
+    P = oracle.Problem(logits=host, V=z.shape[1], targets=t, loss_mask=mask, **kw)
+    R, g_ref = oracle.forward_backward(P)
+    logits = to_device(host, dev)
+    out = handle.forward_backward(logits, torch.from_numpy(t).to(dev),
+                                  None if mask is None else torch.from_numpy(mask).to(dev),
+                                  grad="new", want=("logp", "lse", "count"),
+                                  reduction="token_mean" if P.reduction == 1 else "sum",
+                                  denominator=P.denominator, z_alpha=P.z_alpha)
+    torch.cuda.synchronize()
+    return P, R, g_ref, out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 17])
+def test_small_vocab(dev, handle, dtype, V):
+    rng = np.random.default_rng(V)
+    T = 13
+    z = rng.normal(0, 3, size=(T, V))
+    t = rng.integers(0, V, size=T)
+    t[3] = -100
+    P, R, g_ref, out = _tiny_problem(dev, handle, z, t, dtype, z_alpha=0.01)
+    assert handle.device_error() == 0
+    assert rel(float(out.loss[0]), R.total) <= 1e-5 or abs(R.total) < 1e-30
+    check_grad(grad_to_f64(out.grad), g_ref, dtype == "bf16", f"V={V}")
+
+
+def test_all_rows_masked_and_empty(dev, handle):
+    z = np.random.default_rng(0).normal(size=(5, 300))
+    t = np.full(5, -100)
+    P, R, g_ref, out = _tiny_problem(dev, handle, z, t, "bf16")
+    assert torch.all(out.loss == 0) and torch.all(out.grad.float() == 0)
+    assert int(out.count[0]) == 0
+    # T = 0
+    logits = torch.empty((0, 300), dtype=torch.bfloat16, device=dev)
+    out = handle.forward_backward(logits, torch.empty(0, dtype=torch.int64, device=dev), grad="new")
+    torch.cuda.synchronize()
+    assert torch.all(out.loss == 0)
+
+
+def test_neg_inf_logits(dev, handle):
+    V = 40
+    z = np.random.default_rng(1).normal(size=(4, V))
+    z[0, 5] = -np.inf           # active row, a -inf non-target
+    z[1, :] = -np.inf           # ignored row full of -inf
+    z[2, 1:] = -np.inf          # every non-target is -inf: NLL 0, p_t = 1
+    z[2, 0] = 0.5
+    t = np.array([3, -100, 0, 7])
+    P, R, g_ref, out = _tiny_problem(dev, handle, z, t, "bf16")
+    assert handle.device_error() == 0
+    g = grad_to_f64(out.grad)
+    assert np.all(np.isfinite(g))
+    check_grad(g, g_ref, True, "-inf rows")
+    assert rel(float(out.loss[0]), R.total) <= 1e-5
+
+
+def test_bad_target_sets_device_error(dev, handle):
+    from lm_head_vocab_gb300._lib import LMLOSS_ERR_BAD_TARGET
+    z = torch.zeros((3, 64), dtype=torch.bfloat16, device=dev)
+    t = torch.tensor([1, 64, 2], device=dev)
+    out = handle.forward_backward(z, t, grad="new")
+    torch.cuda.synchronize()
+    assert handle.device_error() == LMLOSS_ERR_BAD_TARGET
+    assert handle.device_error() == 0            # read clears it
+    assert torch.isnan(out.loss[0])
+    assert torch.all(out.grad[0].float() != 0) and torch.isnan(out.grad[1].float()).all()
+
+
+def test_bad_segment_sets_device_error(dev, handle):
+    from lm_head_vocab_gb300._lib import LMLOSS_ERR_BAD_SEGMENT
+    T, V = 4, 100
+    z = torch.zeros((T, V), dtype=torch.bfloat16, device=dev)
+    t = torch.tensor([1, 2, 3, 4], device=dev)
+    seg = torch.tensor([0, 0, 1, 5], dtype=torch.int32, device=dev)
+    adv = torch.ones(2, device=dev)
+    old = torch.zeros(T, device=dev)
+    handle.forward_backward(z, t, segment_ids=seg, num_segments=2, advantages=adv, old_logprobs=old,
+                            ce_weight=0.0, grad="new")
+    torch.cuda.synchronize()
+    assert handle.device_error() == LMLOSS_ERR_BAD_SEGMENT

@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--nbuf", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0, help="profiling only: fewer rows than the workload")
     return ap.parse_args()
 
 
@@ -161,10 +162,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ inputs
-def make_problem(wname: str, rank: int, world: int):
-    """This rank's rows of the workload (world x T rows when world > 1)."""
-    import workloads
-    w = workloads.get(wname)
+def make_problem(w, rank: int, world: int):
+    """This rank's rows of workload w (a batch world x T rows tall when world > 1)
+    and the global active-row count, computed on the host from the seeds."""
     if w.has_gspo:
         raise SystemExit("bench: the GSPO workload needs oracle log-probs for its inputs; "
                          "benchmark it through tests, not here")
@@ -228,7 +228,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w, x, u, targets, mask, n_glob = make_problem(args.workload, 0, 1)
+    import workloads
+    w, x, u, targets, mask, n_glob = make_problem(workloads.get(args.workload), 0, 1)
     per_step = []
     for i in range(args.warmup + args.steps):
         v, cores, desc = oracle_sample_time(w, x, u, targets, mask, args.cpu_seconds / 4)
@@ -263,7 +264,11 @@ def run_ours(args):
     __graft_entry__.build()
     from lm_head_vocab_gb300 import LMLoss
 
-    w, x, u, targets, mask, n_glob = make_problem(args.workload, rank, world)
+    import workloads
+    wl = workloads.get(args.workload)
+    if args.rows:
+        wl = wl.with_shape(args.rows, wl.V)
+    w, x, u, targets, mask, n_glob = make_problem(wl, rank, world)
     kw = call_kwargs(w, world, n_glob)
 
     def to_dev(a):

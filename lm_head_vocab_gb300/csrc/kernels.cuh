@@ -17,6 +17,11 @@
 namespace lmloss {
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool B>
+struct BoolConst {
+    static constexpr bool value = B;
+};
 constexpr long long kWaitLimitCycles = 4000000000LL;   // ~2 s at the top SM clock
 
 // Device error codes (match lmloss_status).
@@ -231,8 +236,14 @@ struct Workspace {
     unsigned long long* seg_absq;  // [max_S] coarse sum of |log-ratio|, 2^-8 units
     int* seg_nonfinite;  // [max_S * 3] +inf, -inf, NaN counts
     float* seg_coef;     // [max_S] per-segment gradient coefficient kappa_i
+    int* row_counter;    // [1] dynamic row hand-out of the fused kernel
+    long long* cnt_part; // [kRedBlocks] per-block active counts
+    double* red_part;    // [kRedBlocks * 3] per-block loss sums
+    unsigned* done;      // [2] blocks finished (count, reduce); back to 0 after each call
     int* err;            // [1]
 };
+
+constexpr int kRedBlocks = 64;   // blocks of the count and reduce kernels
 
 struct CallParams {
     const void* logits;
@@ -272,6 +283,17 @@ __device__ __forceinline__ bool row_active(const CallParams& p, int64_t r, int64
     return t != -100 && (p.mask == nullptr || p.mask[r] != 0);
 }
 
+// Target of row r as an int, -100 when the row takes no part; out-of-range
+// targets keep a value outside [0, V) (clamped into int range).
+__device__ __forceinline__ int row_target(const CallParams& p, int64_t r)
+{
+    int64_t t;
+    if (!row_active(p, r, t)) return -100;
+    if (t < 0) return -1;
+    if (t >= p.V) return 0x7fffffff;
+    return static_cast<int>(t);
+}
+
 // Token scale s: 1/N_active (token mean, 0 if none) or 1/denominator (SUM).
 __device__ __forceinline__ float token_scale(const CallParams& p)
 {
@@ -298,21 +320,26 @@ __device__ __forceinline__ void row_interior(const void* base, int64_t r, int64_
 }
 
 // ======================================================================
-// K0: count active rows, validate targets, clear the segment accumulators.
-// One CTA; deterministic (integer sums).
+// K0: count active rows, validate targets, clear the per-call accumulators.
+// Block b counts a fixed chunk of rows; the last block to finish adds the
+// block counts in block order.  Integer sums: deterministic.
 // ======================================================================
-__global__ void __launch_bounds__(1024) count_kernel(const CallParams p)
+__global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 {
-    __shared__ long long part[32];
+    __shared__ long long part[8];
+    __shared__ bool last;
+    const int tid = threadIdx.x, nb = gridDim.x;
+    const int64_t chunk = (p.T + nb - 1) / nb;
+    const int64_t r0 = blockIdx.x * chunk, r1 = min(p.T, r0 + chunk);
     long long n = 0;
-    for (int64_t r = threadIdx.x; r < p.T; r += blockDim.x) {
+    for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
         int64_t t;
         if (row_active(p, r, t)) {
             ++n;
             if (t < 0 || t >= p.V) set_error(p.ws.err, kErrBadTarget);
         }
     }
-    for (int i = threadIdx.x; i < p.num_segments; i += blockDim.x) {
+    for (int i = blockIdx.x * blockDim.x + tid; i < p.num_segments; i += nb * blockDim.x) {
         p.ws.seg_n[i] = 0;
         p.ws.seg_dq[i] = 0ull;
         p.ws.seg_absq[i] = 0ull;
@@ -322,17 +349,27 @@ __global__ void __launch_bounds__(1024) count_kernel(const CallParams p)
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = n;
+    if ((tid & 31) == 0) part[tid >> 5] = n;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        long long v = (threadIdx.x < (blockDim.x >> 5)) ? part[threadIdx.x] : 0;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (threadIdx.x == 0) {
-            *p.ws.n_active = v;
+    if (tid == 0) {
+        long long v = 0;
+        for (int k = 0; k < (blockDim.x >> 5); ++k) v += part[k];
+        p.ws.cnt_part[blockIdx.x] = v;
+        if (blockIdx.x == 0) {
             *p.ws.n_nonempty = 0;
             *p.ws.gspo_sum = 0.0;
+            *p.ws.row_counter = 0;
         }
+        __threadfence();
+        last = atomicAdd(&p.ws.done[0], 1u) == static_cast<unsigned>(nb - 1);
+    }
+    __syncthreads();
+    if (last && tid == 0) {
+        __threadfence();
+        long long tot = 0;
+        for (int k = 0; k < nb; ++k) tot += *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[k]);
+        *p.ws.n_active = tot;
+        p.ws.done[0] = 0u;
     }
 }
 
@@ -342,14 +379,39 @@ __global__ void __launch_bounds__(1024) count_kernel(const CallParams p)
 // A cluster of C CTAs owns one row at a time; CTA k of the cluster owns the
 // columns [k*slice, (k+1)*slice).  Each CTA stages its slice (and the teacher
 // slice) in shared memory with one bulk copy per row, nbuf rows ahead, then
-//   pass A: maximum over the slice (packed bf16x2 max),
-//   pass B: sum of exp(z - m) over non-target columns (+ teacher sums),
-// merges those partials across the CTA, publishes one record per CTA,
-// synchronises the cluster, reads every CTA's record through distributed
-// shared memory, and writes the gradient of its slice from the staged copy.
-// The row is read from HBM once and the gradient written once.
+//   pass A: maximum over its non-target columns (packed bf16x2 max),
+//   pass B: sum of 2^((z - m) log2 e) over non-target columns, relative to
+//           the CTA maximum (+ teacher max, sum and cross term),
+// publishes one record per CTA, synchronises the cluster, and one warp reads
+// every CTA's record through distributed shared memory, merges them in rank
+// order and forms the row's scalars in double precision.  Pass C then writes
+// the gradient of the slice from the staged copy.  The row is read from HBM
+// once and the gradient written once.
+//
+// Rows are handed out dynamically: rank 0 of each cluster claims the row for
+// a later iteration from a global counter and passes it to its peers in its
+// record, so clusters that share SMs with others do not set the pace.
 // ======================================================================
-constexpr int kHdrBytes = 1024;   // mbarriers, cluster records, warp scratch
+constexpr int kHdrBytes = 2048;   // mbarriers, row queue, cluster records, warp scratch
+constexpr int kMaxCluster = 16;
+
+struct ClusterRec {     // one CTA's partial for the current row (32 bytes)
+    float m, s;         // CTA max over its non-target columns; sum e^(z - m)
+    float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
+    float zt;           // target logit (on the CTA that owns the target column)
+    int next_row;       // rank 0: row for iteration i + nbuf
+    int next_t;         // rank 0: its target, or -100 when the row is inactive
+};
+static_assert(sizeof(ClusterRec) == 32, "record is two 16-byte pushes");
+
+struct RowCoef {        // the row's gradient coefficients, shared by the CTA's threads
+    float cz;           // non-teacher: g_j = sign * 2^(z_j log2e - cz)
+    float lseL, luL;    // teacher: p_j = 2^(z_j log2e - lseL), q_j = 2^(u_j log2e - luL)
+    float a, b;         // teacher: g_j = a p_j - b q_j
+    float gt;           // target column (teacher: minus b q_t still to apply)
+    int neg;            // sign of a
+    int pad;
+};
 
 template <bool BF16, bool KL, int NT>
 __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel(const CallParams p)
@@ -361,20 +423,26 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
     static_assert(NW <= 32, "at most 32 warps");
 
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);                  // [2]
-    Part* rec = reinterpret_cast<Part*>(smem + 64);                       // [2]
-    Part* wpart = reinterpret_cast<Part*>(smem + 64 + 2 * sizeof(Part));  // [NW]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);                  // [2] staged-row copies
+    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + 16);             // [2] cluster records, by row parity
+    int* rowq = reinterpret_cast<int*>(smem + 32);                       // [4] row of iteration i (i & 3)
+    int* tq = reinterpret_cast<int*>(smem + 48);                         // [4] its target (-100: inactive)
+    float* slot = reinterpret_cast<float*>(smem + 64);                   // [1] target logit
+    RowCoef* coef = reinterpret_cast<RowCoef*>(smem + 96);               // [1]
+    float* wred = reinterpret_cast<float*>(smem + 256);                  // [5][32]
+    ClusterRec* rec = reinterpret_cast<ClusterRec*>(smem + 1024);        // [2][kMaxCluster]
     unsigned char* bufs = smem + kHdrBytes;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_rank();
     const int C = p.cluster;
-    const int64_t cid = blockIdx.x / C;
-    const int64_t G = gridDim.x / C;
+    const int cid = static_cast<int>(blockIdx.x) / C;
+    const int G = static_cast<int>(gridDim.x) / C;
     const int64_t c0 = min(p.V, static_cast<int64_t>(rank) * p.slice);
     const int64_t c1 = min(p.V, c0 + p.slice);
     const int nbuf = p.nbuf;
+    const float s_tok = token_scale(p);
 
     auto buf_addr = [&](int b, int a) -> uint32_t {
         return smem_addr(bufs + (static_cast<size_t>(b) * (KL ? 2 : 1) + a) * p.buf_bytes);
@@ -383,14 +451,19 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 
     if (tid == 0) {
         for (int b = 0; b < nbuf; ++b) mbar_init(bar_addr(b), 1);
+        mbar_init(smem_addr(&rbar[0]), 1);
+        mbar_init(smem_addr(&rbar[1]), 1);
+        for (int k = 0; k < 4; ++k) {
+            rowq[k] = (k < nbuf) ? cid + k * G : 0x7fffffff;
+            tq[k] = (k < nbuf && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
+        }
         fence_mbar_init();
     }
-    __syncthreads();
+    cluster_sync_all();   // every peer's record barriers exist before anyone pushes
 
     // Producer side (thread 0): stage row rr's slice into buffer b.
-    auto issue = [&](int64_t rr, int b) {
-        int64_t t;
-        const bool act = row_active(p, rr, t);
+    auto issue = [&](int64_t rr, int tt, int b) {
+        const bool act = tt != -100;
         int64_t e0, e1;
         row_interior<ESZ>(p.logits, rr, p.ld, c0, c1, e0, e1);
         const uint32_t bytes = static_cast<uint32_t>((e1 - e0) * ESZ);
@@ -405,67 +478,45 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             bulk_load(buf_addr(b, 1), static_cast<const unsigned char*>(p.teacher) + off, bytes, bar_addr(b));
     };
 
-    const float s_tok = token_scale(p);
-    bool failed = false;
-
     if (tid == 0)
-        for (int k = 0; k < nbuf - 1; ++k) {
-            const int64_t rr = cid + k * G;
-            if (rr < p.T) issue(rr, k);
-        }
+        for (int k = 0; k < nbuf - 1; ++k)
+            if (rowq[k] < p.T) issue(rowq[k], tq[k], k);
 
-    int nrec = 0;
-    for (int64_t i = 0;; ++i) {
-        const int64_t r = cid + i * G;
+    bool failed = false;
+    for (int i = 0;; ++i) {
+        const int64_t r = rowq[i & 3];
         if (r >= p.T) break;
-        __syncthreads();   // every thread is done with the buffer about to be refilled
+        __syncthreads();   // buffers, scratch and coefficients of the previous row are free
+        int claim_row = 0;
         if (tid == 0) {
-            const int64_t rr = cid + (i + nbuf - 1) * G;
-            if (rr < p.T) issue(rr, static_cast<int>((i + nbuf - 1) % nbuf));
+            const int j = (i + nbuf - 1) & 3;
+            if (rowq[j] < p.T) issue(rowq[j], tq[j], (i + nbuf - 1) % nbuf);
+            if (rank == 0) claim_row = nbuf * G + atomicAdd(p.ws.row_counter, 1);
         }
-        const int b = static_cast<int>(i % nbuf);
+        const int b = i % nbuf;
         const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
 
-        int64_t t;
-        const bool act = row_active(p, r, t);
+        const int64_t t = tq[i & 3];
+        const bool act = t != -100;
         const bool bad = act && (t < 0 || t >= p.V);
         int64_t e0, e1;
         row_interior<ESZ>(p.logits, r, p.ld, c0, c1, e0, e1);
         const int nvec = static_cast<int>((e1 - e0) / VN);
         const size_t row_off = static_cast<size_t>(r * p.ld) * ESZ;
+        const uint32_t bz = buf_addr(b, 0);
+        const uint32_t bu = KL ? buf_addr(b, 1) : 0u;
+        const int64_t tv = t - e0;   // target offset within the interior (may be outside)
+        const bool owner = act && t >= c0 && t < c1;
 
         if (!failed && !mbar_wait_bounded(bar_addr(b), parity, kWaitLimitCycles)) {
             set_error(p.ws.err, kErrTimeout);
             failed = true;
         }
 
-        if (!act) {
-            if (p.grad) {
-                unsigned char* g = static_cast<unsigned char*>(p.grad) + row_off + static_cast<size_t>(e0) * ESZ;
-                for (int v = tid; v < nvec; v += NT) stg128(g + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
-                if (tid == NT - 1) {
-                    for (int64_t j = c0; j < e0; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
-                    for (int64_t j = e1; j < c1; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
-                }
-            }
-            if (rank == 0 && tid == 0) {
-                p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f;
-                if (p.logp_out) p.logp_out[r] = 0.f;
-                if (p.lse_out) p.lse_out[r] = 0.f;
-                if (p.kl_out) p.kl_out[r] = 0.f;
-            }
-            continue;
-        }
-
-        const uint32_t bz = buf_addr(b, 0);
-        const uint32_t bu = KL ? buf_addr(b, 1) : 0u;
-        const int64_t tv = t - e0;   // target offset within the interior (may be outside)
-
-        // ---- pass A: maxima
-        Part P = part_empty();
-        {
+        // ---- pass A: maxima (non-target for z, all columns for u)
+        if (act) {
             uint32_t accz = IO::max_init(), accu = IO::max_init();
-            float mz_extra = -INFINITY;
+            float mx = -INFINITY, mu = -INFINITY;
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
@@ -474,43 +525,68 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     float x[VN];
                     IO::unpack(q, x);
 #pragma unroll
-                    for (int j = 0; j < VN; ++j)
-                        if (j != k) mz_extra = fmaxf(mz_extra, x[j]);
+                    for (int j = 0; j < VN; ++j) {
+                        if (j != k) mx = fmaxf(mx, x[j]);
+                        else slot[0] = x[j];
+                    }
                 } else {
                     accz = IO::max_acc(accz, q);
                 }
                 if (KL) accu = IO::max_acc(accu, lds128(bu + v * 16));
             }
-            P.m = fmaxf(IO::max_final(accz), mz_extra);
-            if (KL) P.mu = IO::max_final(accu);
             if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
-                        if (j != t) P.m = fmaxf(P.m, x);
-                        if (KL) P.mu = fmaxf(P.mu, IO::load1(p.teacher, r * p.ld + j));
+                        if (j != t) mx = fmaxf(mx, x);
+                        else slot[0] = x;
+                        if (KL) mu = fmaxf(mu, IO::load1(p.teacher, r * p.ld + j));
                     }
                 }
             }
+            float m = fmaxf(IO::max_final(accz), mx);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (KL) {
+                mu = fmaxf(mu, IO::max_final(accu));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+            }
+            if (lane == 0) {
+                wred[warp] = m;
+                if (KL) wred[32 + warp] = mu;
+            }
         }
-        // ---- pass B: sums (target column excluded from the non-target sum)
-        {
-            const float mL = (P.m == -INFINITY) ? 0.f : P.m * kLog2e;
-            const float muL = (P.mu == -INFINITY) ? 0.f : P.mu * kLog2e;
+        __syncthreads();
+
+        // ---- pass B: sums relative to the CTA maximum
+        float m_cta = -INFINITY, mu_cta = -INFINITY;
+        if (act) {
+            m_cta = (lane < NW) ? wred[lane] : -INFINITY;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
+            if (KL) {
+                mu_cta = (lane < NW) ? wred[32 + lane] : -INFINITY;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
+            }
+            const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
+            const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
             float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f;
 #pragma unroll 2
             for (int v = tid; v < nvec; v += NT) {
                 float x[VN];
                 IO::unpack(lds128(bz + v * 16), x);
-                const int64_t k = tv - static_cast<int64_t>(v) * VN;
                 float e[VN];
 #pragma unroll
                 for (int j = 0; j < VN; ++j) e[j] = ex2(fmaf(x[j], kLog2e, -mL));
+                const int64_t k = tv - static_cast<int64_t>(v) * VN;
                 if (k >= 0 && k < VN) {
 #pragma unroll
                     for (int j = 0; j < VN; ++j)
-                        if (j == k) { P.zt = x[j]; P.has_t = 1; e[j] = 0.f; }
+                        if (j == k) e[j] = 0.f;
                 }
 #pragma unroll
                 for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
@@ -525,121 +601,249 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     }
                 }
             }
-            P.s = s0 + s1;
-            if (KL) { P.su = su; P.w = w; }
+            float s = s0 + s1;
             if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
-                        if (j == t) { P.zt = x; P.has_t = 1; }
-                        else P.s += ex2(fmaf(x, kLog2e, -mL));
+                        if (j != t) s += ex2(fmaf(x, kLog2e, -mL));
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             const float eu = ex2(fmaf(y, kLog2e, -muL));
-                            P.su += eu;
-                            P.w += (eu > 0.f) ? eu * (y - x) : 0.f;
+                            su += eu;
+                            w += (eu > 0.f) ? eu * (y - x) : 0.f;
                         }
                     }
                 }
             }
-        }
-        // ---- merge: warp, CTA, then the cluster through distributed shared memory
-        P = warp_merge<KL>(P);
-        if (lane == 0) wpart[warp] = P;
-        __syncthreads();
-        if (warp == 0) {
-            Part q = (lane < NW) ? wpart[lane] : part_empty();
-            q = warp_merge<KL>(q);
-            if (lane == 0) rec[nrec & 1] = q;
-        }
-        cluster_sync_all();
-        Part R = part_empty();
-        {
-            Part mine = part_empty();
-            if (lane < C) {
-                const uint32_t base = dsmem_map(smem_addr(&rec[nrec & 1]), static_cast<uint32_t>(lane));
-                mine.m = dsmem_ld_f32(base + offsetof(Part, m));
-                mine.s = dsmem_ld_f32(base + offsetof(Part, s));
-                if (KL) {
-                    mine.mu = dsmem_ld_f32(base + offsetof(Part, mu));
-                    mine.su = dsmem_ld_f32(base + offsetof(Part, su));
-                    mine.w = dsmem_ld_f32(base + offsetof(Part, w));
-                }
-                mine.zt = dsmem_ld_f32(base + offsetof(Part, zt));
-                mine.has_t = static_cast<int>(dsmem_ld_u32(base + offsetof(Part, has_t)));
-            }
-            // fixed order over cluster ranks: identical in every warp of every CTA
-            for (int c = 0; c < C; ++c) {
-                Part q;
-                q.m = __shfl_sync(0xffffffffu, mine.m, c);
-                q.s = __shfl_sync(0xffffffffu, mine.s, c);
-                q.mu = KL ? __shfl_sync(0xffffffffu, mine.mu, c) : -INFINITY;
-                q.su = KL ? __shfl_sync(0xffffffffu, mine.su, c) : 0.f;
-                q.w = KL ? __shfl_sync(0xffffffffu, mine.w, c) : 0.f;
-                q.zt = __shfl_sync(0xffffffffu, mine.zt, c);
-                q.has_t = __shfl_sync(0xffffffffu, mine.has_t, c);
-                if (c == 0) R = q;
-                else part_merge<KL>(R, q);
-            }
-        }
-        ++nrec;
-        const RowScalars S = row_scalars<KL>(R, bad);
-
-        // ---- pass C: gradient, written once
-        if (p.grad) {
-            const float zcoef = 2.f * p.alpha * S.lse;
-            const float a = s_tok * (p.w_ce + zcoef + p.w_kl);    // on p_j
-            const float bq = s_tok * p.w_kl;                       // on q_j
-            const float gt_base = s_tok * p.w_ce * S.tg + s_tok * (zcoef + p.w_kl) * S.p_t;
-            const float lseL = S.lse * kLog2e;
-            const float luL = S.lse_u * kLog2e;
-            unsigned char* g = static_cast<unsigned char*>(p.grad) + row_off + static_cast<size_t>(e0) * ESZ;
-#pragma unroll 2
-            for (int v = tid; v < nvec; v += NT) {
-                float x[VN], gv[VN];
-                IO::unpack(lds128(bz + v * 16), x);
 #pragma unroll
-                for (int j = 0; j < VN; ++j) gv[j] = a * ex2(fmaf(x[j], kLog2e, -lseL));
-                float qv[VN];
+            for (int off = 16; off > 0; off >>= 1) {
+                s += __shfl_xor_sync(0xffffffffu, s, off);
                 if (KL) {
-                    float y[VN];
+                    su += __shfl_xor_sync(0xffffffffu, su, off);
+                    w += __shfl_xor_sync(0xffffffffu, w, off);
+                }
+            }
+            if (lane == 0) {
+                wred[64 + warp] = s;
+                if (KL) { wred[96 + warp] = su; wred[128 + warp] = w; }
+            }
+        }
+        __syncthreads();
+
+        // ---- publish this CTA's record
+        if (warp == 0) {
+            float s = 0.f, su = 0.f, w = 0.f;
+            if (act) {
+                s = (lane < NW) ? wred[64 + lane] : 0.f;
+                if (KL) {
+                    su = (lane < NW) ? wred[96 + lane] : 0.f;
+                    w = (lane < NW) ? wred[128 + lane] : 0.f;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    s += __shfl_xor_sync(0xffffffffu, s, off);
+                    if (KL) {
+                        su += __shfl_xor_sync(0xffffffffu, su, off);
+                        w += __shfl_xor_sync(0xffffffffu, w, off);
+                    }
+                }
+            }
+            if (lane == 0) {
+                ClusterRec R;
+                // the sums were taken against round(m log2e); undo that rounding exactly
+                const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
+                const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
+                R.m = m_cta;
+                R.s = (m_cta == -INFINITY) ? s : s * ex2(-fmaf(m_cta, kLog2e, -mL));
+                R.mu = mu_cta;
+                const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, kLog2e, -muL));
+                R.su = su * fu;
+                R.w = w * fu;
+                R.zt = owner ? slot[0] : 0.f;
+                R.next_row = (rank == 0) ? claim_row : 0;
+                R.next_t = (rank == 0 && claim_row < p.T) ? row_target(p, claim_row) : -100;
+                // push the record into slot [i & 1][rank] of every CTA of the cluster;
+                // the bytes complete on that CTA's record barrier for this parity
+                const uint4* Rv = reinterpret_cast<const uint4*>(&R);
+                const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
+                const uint32_t my_bar = smem_addr(&rbar[i & 1]);
+                mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C * sizeof(ClusterRec)));
+                for (int c = 0; c < C; ++c) {
+                    const uint32_t dst = dsmem_map(my_slot, static_cast<uint32_t>(c));
+                    const uint32_t bar = dsmem_map(my_bar, static_cast<uint32_t>(c));
+                    st_async_v4(dst, Rv[0], bar);
+                    st_async_v4(dst + 16, Rv[1], bar);
+                }
+            }
+        }
+
+        // ---- merge the cluster's records (one warp), row scalars in double
+        if (warp == 0) {
+            if (!failed && !mbar_wait_cluster_bounded(smem_addr(&rbar[i & 1]), static_cast<uint32_t>((i >> 1) & 1),
+                                                      kWaitLimitCycles)) {
+                set_error(p.ws.err, kErrTimeout);
+                failed = true;
+            }
+            ClusterRec q;
+            q.m = -INFINITY; q.s = 0.f; q.mu = -INFINITY; q.su = 0.f; q.w = 0.f; q.zt = 0.f;
+            q.next_row = 0; q.next_t = -100;
+            if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
+            const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
+            const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
+            if (act) {
+                float M = q.m;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float S = q.s * rescale(q.m, M);
+                float Mu = q.mu, Su = 0.f, W = 0.f;
+                if (KL) {
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
+                    const float f = rescale(q.mu, Mu);
+                    Su = q.su * f;
+                    W = q.w * f;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    S += __shfl_xor_sync(0xffffffffu, S, off);
+                    if (KL) {
+                        Su += __shfl_xor_sync(0xffffffffu, Su, off);
+                        W += __shfl_xor_sync(0xffffffffu, W, off);
+                    }
+                }
+                const int own = bad ? 0 : static_cast<int>(t / p.slice);
+                const float ztf = __shfl_sync(0xffffffffu, q.zt, own);
+                if (lane == 0) {
+                    // fp32 throughout, arranged so that no step cancels:
+                    //   lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S  (M - z_t exact),
+                    //   NLL = softplus(d),  lse = lse_nt + softplus(-d)
+                    const float zt = bad ? __int_as_float(0x7fc00000) : ztf;
+                    const float lnS = (S == 0.f) ? -INFINITY : logf(S);
+                    const float d = (M - zt) + lnS;
+                    const float nll = (d > 0.f) ? d + log1pf(expf(-d)) : log1pf(expf(d));
+                    const float sp_neg = (d > 0.f) ? log1pf(expf(-d)) : -d + log1pf(expf(d));  // softplus(-d)
+                    float lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
+                    if (isnan(d)) lse = d;
+                    const float pt = expf(-nll);
+                    const float tg = (pt < 0.25f) ? pt - 1.0f : expm1f(-nll);
+                    float kl = 0.f, dlu = 0.f;
+                    if (KL) {
+                        // lse_u - lse = (Mu - M) + (ln Su - ln S) - softplus(-d)
+                        dlu = ((Mu - M) + (logf(Su) - lnS)) - sp_neg;
+                        if (S == 0.f) dlu = (Mu + logf(Su)) - zt;
+                        kl = W / Su - dlu;
+                    }
+                    const float s = s_tok;
+                    const float zc = 2.f * p.alpha * lse;
+                    const float a = s * (p.w_ce + zc + p.w_kl);
+                    RowCoef cf;
+                    // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
+                    const float lseL = lse * kLog2e;
+                    const float lseL_err = fmaf(lse, kLog2e, -lseL);
+                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2f(fabsf(a)));
+                    cf.neg = a < 0.f;
+                    cf.lseL = lseL;
+                    cf.luL = (lse + dlu) * kLog2e;
+                    cf.a = a;
+                    cf.b = s * p.w_kl;
+                    cf.gt = s * p.w_ce * tg + s * (zc + p.w_kl) * pt;
+                    cf.pad = 0;
+                    *coef = cf;
+                    if (rank == 0) {
+                        p.ws.row_nll[r] = nll;
+                        p.ws.row_lse[r] = lse;
+                        p.ws.row_kl[r] = kl;
+                        if (p.logp_out) p.logp_out[r] = -nll;
+                        if (p.lse_out) p.lse_out[r] = lse;
+                        if (p.kl_out) p.kl_out[r] = kl;
+                    }
+                }
+            } else if (lane == 0 && rank == 0) {
+                p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f;
+                if (p.logp_out) p.logp_out[r] = 0.f;
+                if (p.lse_out) p.lse_out[r] = 0.f;
+                if (p.kl_out) p.kl_out[r] = 0.f;
+            }
+            if (lane == 0) {
+                rowq[(i + nbuf) & 3] = next_row;
+                tq[(i + nbuf) & 3] = next_t;
+            }
+        }
+        __syncthreads();
+
+        // ---- pass C: gradient of the slice, written once
+        if (p.grad) {
+            unsigned char* g = static_cast<unsigned char*>(p.grad) + row_off + static_cast<size_t>(e0) * ESZ;
+            if (!act) {
+                for (int v = tid; v < nvec; v += NT) stg128(g + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
+                if (tid == NT - 1) {
+                    for (int64_t j = c0; j < e0; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
+                    for (int64_t j = e1; j < c1; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
+                }
+                continue;
+            }
+            const RowCoef cf = *coef;
+            if (KL) {
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    float x[VN], y[VN], gv[VN], qv[VN];
+                    IO::unpack(lds128(bz + v * 16), x);
                     IO::unpack(lds128(bu + v * 16), y);
 #pragma unroll
                     for (int j = 0; j < VN; ++j) {
-                        qv[j] = ex2(fmaf(y[j], kLog2e, -luL));
-                        gv[j] -= bq * qv[j];
+                        qv[j] = cf.b * ex2(fmaf(y[j], kLog2e, -cf.luL));
+                        gv[j] = fmaf(cf.a, ex2(fmaf(x[j], kLog2e, -cf.lseL)), -qv[j]);
                     }
-                }
-                const int64_t k = tv - static_cast<int64_t>(v) * VN;
-                if (k >= 0 && k < VN) {
+                    const int64_t k = tv - static_cast<int64_t>(v) * VN;
+                    if (k >= 0 && k < VN) {
 #pragma unroll
-                    for (int j = 0; j < VN; ++j)
-                        if (j == k) gv[j] = gt_base - (KL ? bq * qv[j] : 0.f);
+                        for (int j = 0; j < VN; ++j)
+                            if (j == k) gv[j] = cf.gt - qv[j];
+                    }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                 }
-                stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+            } else {
+                auto body = [&](auto NEG) {
+#pragma unroll 2
+                    for (int v = tid; v < nvec; v += NT) {
+                        float x[VN], gv[VN];
+                        IO::unpack(lds128(bz + v * 16), x);
+#pragma unroll
+                        for (int j = 0; j < VN; ++j) {
+                            const float e = ex2(fmaf(x[j], kLog2e, -cf.cz));
+                            gv[j] = decltype(NEG)::value ? -e : e;
+                        }
+                        const int64_t k = tv - static_cast<int64_t>(v) * VN;
+                        if (k >= 0 && k < VN) {
+#pragma unroll
+                            for (int j = 0; j < VN; ++j)
+                                if (j == k) gv[j] = cf.gt;
+                        }
+                        stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                    }
+                };
+                if (cf.neg) body(BoolConst<true>{});
+                else body(BoolConst<false>{});
             }
             if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
-                        float q = 0.f;
-                        if (KL) q = ex2(fmaf(IO::load1(p.teacher, r * p.ld + j), kLog2e, -luL));
-                        float gj = (j == t) ? gt_base : a * ex2(fmaf(x, kLog2e, -lseL));
-                        gj -= bq * q;
+                        float gj;
+                        if (KL) {
+                            const float qj = cf.b * ex2(fmaf(IO::load1(p.teacher, r * p.ld + j), kLog2e, -cf.luL));
+                            gj = (j == t) ? cf.gt - qj : fmaf(cf.a, ex2(fmaf(x, kLog2e, -cf.lseL)), -qj);
+                        } else {
+                            const float e = ex2(fmaf(x, kLog2e, -cf.cz));
+                            gj = (j == t) ? cf.gt : (cf.neg ? -e : e);
+                        }
                         IO::store1(p.grad, r * p.ld + j, gj);
                     }
                 }
             }
-        }
-        if (rank == 0 && tid == 0) {
-            p.ws.row_nll[r] = S.nll;
-            p.ws.row_lse[r] = S.lse;
-            p.ws.row_kl[r] = S.kl;
-            if (p.logp_out) p.logp_out[r] = -S.nll;
-            if (p.lse_out) p.lse_out[r] = S.lse;
-            if (p.kl_out) p.kl_out[r] = S.kl;
         }
     }
     cluster_sync_all();   // no CTA leaves while a peer may still read its records
@@ -650,7 +854,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 // per row at a time, online max/sum in registers, no staging.
 // ======================================================================
 template <bool BF16, bool KL, int NT>
-__global__ void __launch_bounds__(NT) stats_kernel(const CallParams p)
+__global__ void __launch_bounds__(NT, 2) stats_kernel(const CallParams p)
 {
     using IO = Vec<BF16>;
     constexpr int VN = IO::N;
@@ -706,16 +910,31 @@ __global__ void __launch_bounds__(NT) stats_kernel(const CallParams p)
                 P.w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
             }
         };
-#pragma unroll 4
-        for (int v = tid; v < nvec; v += NT) {
-            float x[VN];
-            IO::unpack(ldg_stream(zrow + static_cast<size_t>(v) * 16), x);
-            const int64_t k = tv - static_cast<int64_t>(v) * VN;
-            add_z(x, (k >= 0 && k < VN) ? k : -1);
-            if (KL) {
-                float y[VN];
-                IO::unpack(ldg_stream(urow + static_cast<size_t>(v) * 16), y);
-                add_u(x, y);
+        // four independent 16-byte loads in flight per thread before any arithmetic
+        constexpr int U = 4;
+        for (int v0 = tid; v0 < nvec; v0 += U * NT) {
+            uint4 qz[U], qu[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int v = v0 + k * NT;
+                if (v < nvec) {
+                    qz[k] = ldg_stream(zrow + static_cast<size_t>(v) * 16);
+                    if (KL) qu[k] = ldg_stream(urow + static_cast<size_t>(v) * 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int v = v0 + k * NT;
+                if (v >= nvec) break;
+                float x[VN];
+                IO::unpack(qz[k], x);
+                const int64_t kk = tv - static_cast<int64_t>(v) * VN;
+                add_z(x, (kk >= 0 && kk < VN) ? kk : -1);
+                if (KL) {
+                    float y[VN];
+                    IO::unpack(qu[k], y);
+                    add_u(x, y);
+                }
             }
         }
         if (tid == NT - 1) {
@@ -854,7 +1073,7 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
 // s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot) once per element.
 // ======================================================================
 template <bool BF16, int NT>
-__global__ void __launch_bounds__(NT) grad_kernel(const CallParams p)
+__global__ void __launch_bounds__(NT, 2) grad_kernel(const CallParams p)
 {
     using IO = Vec<BF16>;
     constexpr int VN = IO::N;
@@ -891,19 +1110,30 @@ __global__ void __launch_bounds__(NT) grad_kernel(const CallParams p)
         const float gt = (s_tok * p.w_ce + c_r) * tg + s_tok * zcoef * p_t;
         const float lseL = lse * kLog2e;
         const int64_t tv = t - e0;
-#pragma unroll 4
-        for (int v = tid; v < nvec; v += NT) {
-            float x[VN], gv[VN];
-            IO::unpack(ldg_stream(zrow + static_cast<size_t>(v) * 16), x);
+        constexpr int U = 4;
+        for (int v0 = tid; v0 < nvec; v0 += U * NT) {
+            uint4 qz[U];
 #pragma unroll
-            for (int j = 0; j < VN; ++j) gv[j] = a * ex2(fmaf(x[j], kLog2e, -lseL));
-            const int64_t k = tv - static_cast<int64_t>(v) * VN;
-            if (k >= 0 && k < VN) {
-#pragma unroll
-                for (int j = 0; j < VN; ++j)
-                    if (j == k) gv[j] = gt;
+            for (int k = 0; k < U; ++k) {
+                const int v = v0 + k * NT;
+                if (v < nvec) qz[k] = ldg_stream(zrow + static_cast<size_t>(v) * 16);
             }
-            stg128(grow + static_cast<size_t>(v) * 16, IO::pack(gv));
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int v = v0 + k * NT;
+                if (v >= nvec) break;
+                float x[VN], gv[VN];
+                IO::unpack(qz[k], x);
+#pragma unroll
+                for (int j = 0; j < VN; ++j) gv[j] = a * ex2(fmaf(x[j], kLog2e, -lseL));
+                const int64_t kk = tv - static_cast<int64_t>(v) * VN;
+                if (kk >= 0 && kk < VN) {
+#pragma unroll
+                    for (int j = 0; j < VN; ++j)
+                        if (j == kk) gv[j] = gt;
+                }
+                stg128(grow + static_cast<size_t>(v) * 16, IO::pack(gv));
+            }
         }
         if (tid == NT - 1) {
             for (int pass = 0; pass < 2; ++pass) {
@@ -918,17 +1148,22 @@ __global__ void __launch_bounds__(NT) grad_kernel(const CallParams p)
 }
 
 // ======================================================================
-// K4: deterministic loss reduction (one CTA, fixed assignment, fp64).
+// K4: deterministic loss reduction.  Block b sums a fixed chunk of rows in a
+// fixed order (fp64); the last block to finish adds the block partials in
+// block order and scales them.
 // xtuner PR 1963 "[FSDP][Loss] Switch gradient reduction to SUM": each term
-// is its sum over tokens times the reduction scale; the z term carries
-// alpha (z-loss diff: loss * z_loss_alpha / batch_size).
+// is its sum over tokens times the reduction scale; the z term carries alpha
+// (z-loss diff: loss * z_loss_alpha / batch_size).
 // ======================================================================
-__global__ void __launch_bounds__(1024) reduce_kernel(const CallParams p)
+__global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
 {
-    __shared__ double part[3][32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    __shared__ double part[3][8];
+    __shared__ bool last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5, nb = gridDim.x;
+    const int64_t chunk = (p.T + nb - 1) / nb;
+    const int64_t r0 = blockIdx.x * chunk, r1 = min(p.T, r0 + chunk);
     double a = 0.0, b = 0.0, c = 0.0;
-    for (int64_t r = tid; r < p.T; r += blockDim.x) {
+    for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
         const double lse = p.ws.row_lse[r];
         a += p.ws.row_nll[r];
         b += lse * lse;
@@ -944,6 +1179,19 @@ __global__ void __launch_bounds__(1024) reduce_kernel(const CallParams p)
     if (tid == 0) {
         double sa = 0.0, sb = 0.0, sc = 0.0;
         for (int k = 0; k < nw; ++k) { sa += part[0][k]; sb += part[1][k]; sc += part[2][k]; }
+        p.ws.red_part[3 * blockIdx.x] = sa;
+        p.ws.red_part[3 * blockIdx.x + 1] = sb;
+        p.ws.red_part[3 * blockIdx.x + 2] = sc;
+        __threadfence();
+        last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
+    }
+    __syncthreads();
+    if (last && tid == 0) {
+        __threadfence();
+        double sa = 0.0, sb = 0.0, sc = 0.0;
+        const volatile double* rp = p.ws.red_part;
+        for (int k = 0; k < nb; ++k) { sa += rp[3 * k]; sb += rp[3 * k + 1]; sc += rp[3 * k + 2]; }
+        p.ws.done[1] = 0u;
         const int64_t n = *p.ws.n_active;
         const double s = (p.reduction == 1) ? (n > 0 ? 1.0 / static_cast<double>(n) : 0.0) : p.inv_denominator;
         const double ce = s * sa;

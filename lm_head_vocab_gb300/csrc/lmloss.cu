@@ -131,24 +131,24 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
     const bool bf16 = a->dtype == LMLOSS_BF16;
     const bool kl = a->teacher_logits != nullptr;
     const int esz = bf16 ? 2 : 4;
-    int NT = h->cfg_threads ? h->cfg_threads : (bf16 ? 512 : 256);
-    int nbuf = h->cfg_nbuf ? h->cfg_nbuf : 2;
+    // Default shape, from a sweep on GB300: one staged row per CTA; the
+    // smallest cluster whose slice (logits, plus teacher) fits in 56 KB (112 KB
+    // with a teacher), so that three (two) CTAs share an SM; and about 110
+    // elements per thread, rounded to 128, 256 or 512 threads.
+    int nbuf = h->cfg_nbuf ? h->cfg_nbuf : 1;
     int C = h->cfg_cluster;
     if (!C) {
-        // smallest cluster whose staged slices leave room for two CTAs per SM,
-        // else the smallest that fits at all
-        const size_t half = static_cast<size_t>(h->smem_optin) / 2 - 1024;
-        for (int c = 1; c <= 16 && !C; ++c)
-            if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= half) C = c;
-        for (int c = 1; c <= 16 && !C; ++c)
-            if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= static_cast<size_t>(h->smem_optin)) C = c;
-        if (!C && !h->cfg_nbuf) {
-            nbuf = 1;
-            for (int c = 1; c <= 16 && !C; ++c)
-                if (fused_smem(a->V, c, nbuf, kl, esz, nullptr, nullptr) <= static_cast<size_t>(h->smem_optin)) C = c;
-        }
-        if (!C) return LMLOSS_ERR_UNSUPPORTED;
+        const int64_t row_bytes = a->V * esz * (kl ? 2 : 1);
+        const int64_t budget = kl ? 112 * 1024 : 56 * 1024;
+        int64_t c = (row_bytes + budget - 1) / budget;
+        C = static_cast<int>(c < 1 ? 1 : (c > 16 ? 16 : c));
     }
+    int NT = h->cfg_threads;
+    if (!NT) {
+        const double per_thread = static_cast<double>((a->V + C - 1) / C) / 110.0;
+        NT = per_thread < 181.0 ? 128 : (per_thread < 362.0 ? 256 : 512);
+    }
+    if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel
     if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
     P.fn = pick_fused(bf16, kl, NT);
     if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
@@ -244,6 +244,8 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     const size_t o_nll = take(4 * T), o_lse = take(4 * T), o_kl = take(4 * T);
     const size_t o_scal = take(64);
     const size_t o_sn = take(4 * S), o_dq = take(8 * S), o_aq = take(8 * S), o_nf = take(12 * S), o_coef = take(4 * S);
+    const size_t o_ctr = take(16);
+    const size_t o_cnt = take(8 * kRedBlocks), o_red = take(24 * kRedBlocks), o_done = take(16);
     const size_t o_err = take(16);
     if (cudaMalloc(&h->ws_mem, off) != cudaSuccess) {
         delete h;
@@ -262,6 +264,10 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     h->ws.seg_absq = reinterpret_cast<unsigned long long*>(base + o_aq);
     h->ws.seg_nonfinite = reinterpret_cast<int*>(base + o_nf);
     h->ws.seg_coef = reinterpret_cast<float*>(base + o_coef);
+    h->ws.row_counter = reinterpret_cast<int*>(base + o_ctr);
+    h->ws.cnt_part = reinterpret_cast<long long*>(base + o_cnt);
+    h->ws.red_part = reinterpret_cast<double*>(base + o_red);
+    h->ws.done = reinterpret_cast<unsigned*>(base + o_done);
     h->ws.err = reinterpret_cast<int*>(base + o_err);
     h->ev = static_cast<cudaEvent_t*>(std::calloc(2 * lmloss_ctx::kMaxTimed, sizeof(cudaEvent_t)));
     if (!h->ev || cudaMemset(h->ws_mem, 0, off) != cudaSuccess) {
@@ -389,7 +395,11 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     lmloss_call_info info{};
     const int NT_STREAM = 512;
 
-    count_kernel<<<1, 1024, 0, stream>>>(p);
+    // count / reduce: one block per 64 rows, at most kRedBlocks, at least one
+    int64_t rb = (a->T + 63) / 64;
+    if (rb > kRedBlocks) rb = kRedBlocks;
+    const int red_blocks = rb < 1 ? 1 : static_cast<int>(rb);
+    count_kernel<<<red_blocks, 256, 0, stream>>>(p);
     if ((st = launch_err()) != LMLOSS_OK) return st;
     info.launches = 1;
 
@@ -482,7 +492,7 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
         cudaEventRecord(h->ev[2 * ev_slot + 1], stream);
         h->ev_used = ev_slot + 1;
     }
-    reduce_kernel<<<1, 1024, 0, stream>>>(p);
+    reduce_kernel<<<red_blocks, 256, 0, stream>>>(p);
     if ((st = launch_err()) != LMLOSS_OK) return st;
     info.launches += 1;
     h->info = info;

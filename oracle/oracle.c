@@ -199,12 +199,14 @@ int orc_forward(int dtype, int64_t n, int64_t V, int64_t ld,
  * -exp(lse_nt - lse) in exact arithmetic; that form is used because p_t - 1
  * cancels to 0 in double once the target dominates ([TT] Numerics).
  * Inactive rows get an all-zero gradient.  c may be NULL (no GSPO term).
+ * gscale (optional, [n, V]) receives the sum of the magnitudes of the terms
+ * above, the scale against which a rounding error in any one term is judged.
  */
 int orc_grad(int dtype, int64_t n, int64_t V, int64_t ld,
              const void* logits, const void* teacher, double temperature,
              const int64_t* targets, const uint8_t* active,
              double s_tok, double w_ce, double alpha, double w_kl, const double* c,
-             double* grad, int nthreads)
+             double* grad, double* gscale, int nthreads)
 {
     int failed = 0;
 #pragma omp parallel num_threads(orc_threads(nthreads))
@@ -220,9 +222,12 @@ int orc_grad(int dtype, int64_t n, int64_t V, int64_t ld,
 #pragma omp for schedule(dynamic, 4)
         for (int64_t r = 0; r < n; ++r) {
             double* g = grad + r * V;
+            double* gs = gscale ? gscale + r * V : NULL;
             if (!ok) continue;
             if (!active[r]) {
                 for (int64_t j = 0; j < V; ++j) g[j] = 0.0;
+                if (gs)
+                    for (int64_t j = 0; j < V; ++j) gs[j] = 0.0;
                 continue;
             }
             int64_t t = targets[r];
@@ -241,12 +246,15 @@ int orc_grad(int dtype, int64_t n, int64_t V, int64_t ld,
                 double p = exp(z[j] - s.lse);
                 double p_minus_onehot = (j == t) ? -exp(s.lse_nt - s.lse) : p;
                 double term = w_ce * p_minus_onehot + 2.0 * alpha * s.lse * p;
+                double mag = fabs(w_ce * p_minus_onehot) + fabs(2.0 * alpha * s.lse * p);
                 if (teacher) {
                     double p_tau = exp(work[V + j] - lse_b);
                     double q = exp(work[j] - lse_a);
                     term += w_kl * (p_tau - q) / temperature;
+                    mag += fabs(w_kl * p_tau / temperature) + fabs(w_kl * q / temperature);
                 }
                 g[j] = s_tok * term + c_r * p_minus_onehot;
+                if (gs) gs[j] = fabs(s_tok) * mag + fabs(c_r * p_minus_onehot);
             }
         }
         free(z);

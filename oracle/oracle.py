@@ -79,7 +79,7 @@ def _load():
         d = ctypes.c_double
         lib.orc_forward.argtypes = [ctypes.c_int, i64, i64, i64, p, p, d, p, p, p, p, p, p, ctypes.c_int]
         lib.orc_forward.restype = ctypes.c_int
-        lib.orc_grad.argtypes = [ctypes.c_int, i64, i64, i64, p, p, d, p, p, d, d, d, d, p, p, ctypes.c_int]
+        lib.orc_grad.argtypes = [ctypes.c_int, i64, i64, i64, p, p, d, p, p, d, d, d, d, p, p, p, ctypes.c_int]
         lib.orc_grad.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -261,8 +261,11 @@ def forward(P: Problem, nthreads: int = 0) -> Result:
                   ce, z, kl_loss, gspo, total, seam, coef)
 
 
-def grad_rows(P: Problem, R: Result, rows: Optional[np.ndarray] = None, nthreads: int = 0) -> np.ndarray:
-    """fp64 gradient [len(rows), V] of the total loss for the given rows (default all)."""
+def grad_rows(P: Problem, R: Result, rows: Optional[np.ndarray] = None, nthreads: int = 0,
+              with_scale: bool = False):
+    """fp64 gradient [len(rows), V] of the total loss for the given rows (default all).
+    with_scale: also return, per element, the sum of the magnitudes of the terms
+    that make up the gradient (a rounding error in one term is judged against it)."""
     lib = _load()
     if rows is None:
         rows = np.arange(P.T)
@@ -273,17 +276,22 @@ def grad_rows(P: Problem, R: Result, rows: Optional[np.ndarray] = None, nthreads
     act = np.ascontiguousarray(R.active[rows], dtype=np.uint8)
     coef = None if R.coef is None else np.ascontiguousarray(R.coef[rows])
     g = np.zeros((len(rows), P.V), dtype=np.float64)
+    gs = np.zeros_like(g) if with_scale else None
     rc = lib.orc_grad(P.dtype, len(rows), P.V, sub.shape[1], _ptr(sub), _ptr(tsub), float(P.temperature),
                       _ptr(targets), _ptr(act), float(R.s_tok), float(P.ce_weight), float(P.z_alpha),
-                      float(P.kl_weight), _ptr(coef), _ptr(g), int(nthreads))
+                      float(P.kl_weight), _ptr(coef), _ptr(g), _ptr(gs), int(nthreads))
     if rc != 0:
         raise MemoryError("oracle: out of host memory")
-    return g
+    return (g, gs) if with_scale else g
 
 
-def forward_backward(P: Problem, nthreads: int = 0):
-    """(Result, fp64 gradient [T, V]) for a small problem."""
+def forward_backward(P: Problem, nthreads: int = 0, with_scale: bool = False):
+    """(Result, fp64 gradient [T, V]) for a small problem; with_scale adds the
+    per-element term magnitudes as a third item."""
     R = forward(P, nthreads)
+    if with_scale:
+        g, gs = grad_rows(P, R, None, nthreads, with_scale=True)
+        return R, g, gs
     return R, grad_rows(P, R, None, nthreads)
 
 

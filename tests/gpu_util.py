@@ -27,23 +27,40 @@ def bf16_ulp(ref: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(a)) - 7)
 
 
-def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bf16: bool, what: str = ""):
-    """bf16: within 1 ulp of the fp64 value (values below 2^-126 may flush to 0);
-    fp32: within 1e-6 absolute.  Exact zeros (inactive rows) must stay exact."""
+# Where a gradient element is the difference of two terms (distillation:
+# a p_j - b q_j), the fp32 kernel cannot land within 1 ulp of a difference that
+# cancels: each term carries a relative error of at most 2^-19 from rounding its
+# exponent argument (half an fp32 ulp at |argument| < 64) plus about 2^-22 from
+# ex2.approx, so the difference is allowed 2^-17 of the terms' summed magnitude
+# (the oracle's per-element "scale") on top of the 1-ulp bound.  Where nothing
+# cancels the allowance is ~2^-9 ulp and changes nothing.
+TERM_ALLOWANCE = 2.0 ** -17
+
+
+def check_grad(g_gpu: np.ndarray, g_ref: np.ndarray, bf16: bool, what: str = "", scale=None):
+    """bf16: within 1 ulp of the fp64 value (values below 2^-126 may flush to 0),
+    plus TERM_ALLOWANCE * scale when the oracle's term magnitudes are given;
+    fp32: within 1e-6 absolute.  Exact zeros (inactive rows) must stay exact.
+    Returns (worst error in ulps, elements that needed the allowance)."""
     assert g_gpu.shape == g_ref.shape
     assert np.all(np.isfinite(g_gpu)), f"{what}: non-finite gradient"
     zero = g_ref == 0.0
+    if scale is not None:
+        zero &= scale == 0.0
     assert np.all(g_gpu[zero] == 0.0), f"{what}: nonzero gradient where the oracle has exact 0"
     err = np.abs(g_gpu - g_ref)
     if bf16:
         tiny = np.abs(g_ref) < BF16_TINY
-        ok = (err <= bf16_ulp(g_ref)) | (tiny & (np.abs(g_gpu) <= BF16_TINY))
-        worst = float(np.max(np.where(tiny, 0.0, err / bf16_ulp(g_ref)))) if g_ref.size else 0.0
-        assert ok.all(), f"{what}: {int((~ok).sum())} elements beyond 1 bf16 ulp (worst {worst:.3f} ulp)"
-        return worst
+        ulp = bf16_ulp(g_ref)
+        allow = 0.0 if scale is None else TERM_ALLOWANCE * scale
+        ok = (err <= ulp + allow) | (tiny & (np.abs(g_gpu) <= BF16_TINY))
+        worst = float(np.max(np.where(tiny, 0.0, err / ulp))) if g_ref.size else 0.0
+        used = int(((err > ulp) & ok & ~tiny).sum())
+        assert ok.all(), f"{what}: {int((~ok).sum())} elements beyond the bound (worst {worst:.3f} ulp)"
+        return worst, used
     worst = float(err.max()) if err.size else 0.0
     assert worst <= 1e-6, f"{what}: max abs error {worst:.3e} > 1e-6"
-    return worst
+    return worst, 0
 
 
 def rel(a, b):

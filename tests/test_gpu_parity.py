@@ -4,7 +4,9 @@ same seeded inputs, element by element.
 Tolerances (from the arithmetic, fixed here):
   losses            relative 1e-5;
   bf16 gradients    within 1 bf16 ulp of the fp64 value (a value below 2^-126
-                    may flush to 0);
+                    may flush to 0); where the gradient is a difference of two
+                    terms (distillation), plus 2^-17 of the terms' summed
+                    magnitude (see tests/gpu_util.py for the derivation);
   fp32 gradients    absolute 1e-6;
   integer outputs   bit-exact (active count, segment counts, segment flags
                     away from a clip bound, masked rows exactly 0).
@@ -50,7 +52,7 @@ def run(handle, case, grad="new", inp=None):
     return inp, out
 
 
-def compare_all(case, out, R, g_ref, what):
+def compare_all(case, out, R, g_ref, what, scale=None):
     bf16 = case.w.dtype == "bf16"
     loss = out.loss.cpu().numpy().astype(np.float64)
     ref = [R.total, R.ce, R.z, R.kl_loss, R.gspo]
@@ -71,7 +73,7 @@ def compare_all(case, out, R, g_ref, what):
     if out.kl is not None:
         np.testing.assert_allclose(out.kl.cpu().numpy()[act], R.kl[act], rtol=1e-4, atol=2e-6)
     if out.grad is not None:
-        check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what)
+        check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what, scale)
 
 
 SMALL = [
@@ -97,9 +99,9 @@ def _case(dev, name, shape):
 @pytest.mark.parametrize("name,shape", SMALL, ids=[f"{n}-{s}" for n, s in SMALL])
 def test_parity_small(dev, handle, name, shape):
     case = _case(dev, name, shape)
-    R, g_ref = oracle.forward_backward(case.P)
+    R, g_ref, scale = oracle.forward_backward(case.P, with_scale=True)
     inp, out = run(handle, case)
-    compare_all(case, out, R, g_ref, f"{name} {shape}")
+    compare_all(case, out, R, g_ref, f"{name} {shape}", scale)
     if case.w.has_gspo:
         sc = out.seg_count.cpu().numpy()
         assert np.array_equal(sc, R.seam.n)
@@ -109,7 +111,8 @@ def test_parity_small(dev, handle, name, shape):
         lo, hi = 1 - case.w.clip_eps_low, 1 + case.w.clip_eps_high
         amb = (np.abs(s - lo) < 1e-6 * lo) | (np.abs(s - hi) < 1e-6 * hi)
         assert np.array_equal(flag[~amb], R.seam.flag[~amb])
-        np.testing.assert_allclose(out.seg_ratio.cpu().numpy()[R.seam.n > 0], s[R.seam.n > 0], rtol=1e-6)
+        # the ratio inherits the fp32 log-probs' error (about 1e-6 of |logp| ~ 12)
+        np.testing.assert_allclose(out.seg_ratio.cpu().numpy()[R.seam.n > 0], s[R.seam.n > 0], rtol=2e-5)
     # in place gives the same bits as out of place
     logits2 = inp["logits"].clone()
     inp2 = dict(inp, logits=logits2)
@@ -133,6 +136,16 @@ def test_confident_rows_properties(dev, handle):
         assert logp[r] < 0.0
         assert g[r, t[r]] < 0.0
         assert abs(g[r].sum()) <= 2.0 ** -8 * np.abs(g[r]).sum()
+
+
+def test_kl_allowance_is_rare(dev, handle):
+    """The distillation gradient needs the cancellation allowance on only a tiny
+    fraction of elements; everything else is within 1 bf16 ulp."""
+    case = _case(dev, "ce_z_kl_bf16", dict(T=32, V=262144))
+    R, g_ref, scale = oracle.forward_backward(case.P, with_scale=True)
+    _, out = run(handle, case)
+    worst, used = check_grad(grad_to_f64(out.grad), g_ref, True, "kl", scale)
+    assert used <= 1e-3 * g_ref.size, used
 
 
 def test_deterministic_repeat(dev, handle):

@@ -22,7 +22,8 @@ MUTATIONS = [
     ("drop_log1p_in_softplus", "if (x > 0.0) return x + log1p(exp(-x));", "if (x > 0.0) return x;"),
     ("target_included_in_sum", "if (j != skip) s += exp(x[j] - m);", "s += exp(x[j] - m);"),
     ("wrong_sign_target_grad", "? -exp(s.lse_nt - s.lse) : p;", "? exp(s.lse_nt - s.lse) : p;"),
-    ("z_grad_missing_factor_2", "2.0 * alpha * s.lse * p", "alpha * s.lse * p"),
+    ("z_grad_missing_factor_2", "double term = w_ce * p_minus_onehot + 2.0 * alpha * s.lse * p;",
+     "double term = w_ce * p_minus_onehot + alpha * s.lse * p;"),
     ("kl_operands_swapped", "term += w_kl * (p_tau - q) / temperature;", "term += w_kl * (q - p_tau) / temperature;"),
     ("kl_wrong_log_term", "kl += q * (log_q - (b[j] - lse_b));", "kl += q * (log_q - (b[j] - lse_a));"),
     ("logaddexp_wrong_sign", "return hi + log1p(exp(lo - hi));", "return hi - log1p(exp(lo - hi));"),

@@ -182,6 +182,32 @@ lmloss_status lmloss_get_timing(lmloss_handle handle, float* total_ms, int32_t* 
 /* Launch shape and kernel count of the last call on this handle. */
 lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info);
 
+/*
+ * Allocation-free variant of lmloss_forward_backward.  The pages have no
+ * counterpart: it is for callers that may not allocate device memory once they
+ * are running, such as an inference-engine plugin whose enqueue step must not
+ * allocate, or a service that plans all of its device memory at start-up,
+ * because cudaMalloc can synchronise the device and can fail under memory
+ * pressure.
+ *
+ * Same arguments, results and asynchrony as lmloss_forward_backward, on the
+ * current device, without a handle.  It allocates nothing: its workspace is a
+ * fixed array of about 0.9 MB inside this library, which every GPU that loads
+ * the library holds until the process exits.  Limits: T <= LMLOSS_NOALLOC_MAX_T
+ * rows and, with GSPO, num_segments <= LMLOSS_NOALLOC_MAX_SEGMENTS; a larger
+ * call returns LMLOSS_ERR_INVALID_ARG before anything is launched.
+ *
+ * The first call on a device looks up the array's device address and the
+ * device's SM limits (no allocation); make that first call before any stream
+ * capture.  Every call on a device shares the one array, which keeps the last
+ * call's contents, so calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.  Device-side data errors
+ * show up only as NaN losses and gradients: there is no handle to read them from.
+ */
+#define LMLOSS_NOALLOC_MAX_T 65536
+#define LMLOSS_NOALLOC_MAX_SEGMENTS 4096
+lmloss_status lmloss_forward_backward_noalloc(const lmloss_args* args, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

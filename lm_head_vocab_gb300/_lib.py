@@ -196,3 +196,20 @@ def lmloss_get_call_info(handle) -> dict:
     if st != LMLOSS_OK:
         raise LMLossError(st, "lmloss_get_call_info")
     return {n: getattr(info, n) for n, _ in lmloss_call_info._fields_}
+
+
+def lmloss_forward_backward_noalloc(args: lmloss_args, stream: int) -> int:
+    """Allocation-free variant of lmloss_forward_backward on the current device.
+
+    For callers that may not allocate device memory once running (an
+    inference-engine plugin whose enqueue step must not allocate, or a service
+    that plans all device memory at start-up).  The workspace is a fixed array
+    inside the library; a call with more than LMLOSS_NOALLOC_MAX_T rows or
+    LMLOSS_NOALLOC_MAX_SEGMENTS segments returns LMLOSS_ERR_INVALID_ARG.  The
+    first call on a device does a one-time look-up (make it before any stream
+    capture); calls that overlap on the GPU share the array and race.
+    """
+    fn = load().lmloss_forward_backward_noalloc
+    fn.argtypes = [ctypes.POINTER(lmloss_args), ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(ctypes.byref(args), ctypes.c_void_p(stream))

@@ -500,3 +500,125 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Allocation-free variant of lmloss_forward_backward.
+//
+// Some callers may not allocate device memory once they are running, for
+// example an inference-engine plugin whose enqueue step must not allocate, or
+// a service that plans every byte of device memory at start-up (cudaMalloc can
+// synchronise the device and can fail under memory pressure).  This entry
+// point takes no handle: its workspace is the fixed array below, which every
+// GPU that loads this library holds until the process exits.
+// ===========================================================================
+#include <mutex>
+
+namespace {
+
+constexpr int64_t kNoAllocMaxT = LMLOSS_NOALLOC_MAX_T;
+constexpr int64_t kNoAllocMaxS = LMLOSS_NOALLOC_MAX_SEGMENTS;
+
+constexpr size_t na_align(size_t x) { return (x + 255) / 256 * 256; }
+
+// Byte offsets of the workspace pieces inside the array.
+struct NoAllocLayout {
+    static constexpr size_t nll = 0;
+    static constexpr size_t lse = nll + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t kl = lse + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t scal = kl + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t seg_n = scal + na_align(64);
+    static constexpr size_t seg_dq = seg_n + na_align(4 * kNoAllocMaxS);
+    static constexpr size_t seg_absq = seg_dq + na_align(8 * kNoAllocMaxS);
+    static constexpr size_t seg_nf = seg_absq + na_align(8 * kNoAllocMaxS);
+    static constexpr size_t seg_coef = seg_nf + na_align(12 * kNoAllocMaxS);
+    static constexpr size_t counter = seg_coef + na_align(4 * kNoAllocMaxS);
+    static constexpr size_t cnt_part = counter + na_align(16);
+    static constexpr size_t red_part = cnt_part + na_align(8 * kRedBlocks);
+    static constexpr size_t done = red_part + na_align(24 * kRedBlocks);
+    static constexpr size_t err = done + na_align(16);
+    static constexpr size_t total = err + na_align(16);
+};
+
+// The workspace itself (about 0.9 MB).  It is zero when the library loads, as
+// the block counters that must start every call at zero require; the kernels
+// return those counters to zero at the end of each call and clear the
+// per-call accumulators themselves at its start.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NoAllocLayout::total];
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+    int smem_optin = 0;
+};
+
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: look up the array's device
+// address (in host code its name only stands in for it) and the SM limits.
+lmloss_status noalloc_setup(int device, NoAllocDevice** out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice& d = g_noalloc_dev[device];
+    if (!d.ready) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return LMLOSS_ERR_CUDA;
+        }
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+            return LMLOSS_ERR_CUDA;
+        d.scratch = static_cast<unsigned char*>(ptr);
+        d.ready = true;
+    }
+    *out = &d;
+    return LMLOSS_OK;
+}
+
+}  // namespace
+
+extern "C" lmloss_status lmloss_forward_backward_noalloc(const lmloss_args* a, cudaStream_t stream)
+{
+    lmloss_status st = check(a);
+    if (st != LMLOSS_OK) return st;
+    if (a->T > kNoAllocMaxT) return LMLOSS_ERR_INVALID_ARG;
+    if (a->segment_ids && a->num_segments > kNoAllocMaxS) return LMLOSS_ERR_INVALID_ARG;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    if (device < 0 || device >= kNoAllocMaxDevices) return LMLOSS_ERR_UNSUPPORTED;
+    NoAllocDevice* d = nullptr;
+    if ((st = noalloc_setup(device, &d)) != LMLOSS_OK) return st;
+
+    // A context on the stack whose workspace is the fixed array: the regular
+    // call path then runs unchanged and allocates nothing.
+    lmloss_ctx ctx;
+    ctx.device = device;
+    ctx.max_T = kNoAllocMaxT;
+    ctx.max_S = static_cast<int32_t>(kNoAllocMaxS);
+    ctx.num_sms = d->num_sms;
+    ctx.smem_optin = d->smem_optin;
+    unsigned char* b = d->scratch;
+    using L = NoAllocLayout;
+    ctx.ws.row_nll = reinterpret_cast<float*>(b + L::nll);
+    ctx.ws.row_lse = reinterpret_cast<float*>(b + L::lse);
+    ctx.ws.row_kl = reinterpret_cast<float*>(b + L::kl);
+    ctx.ws.n_active = reinterpret_cast<int64_t*>(b + L::scal);
+    ctx.ws.n_nonempty = reinterpret_cast<int64_t*>(b + L::scal + 8);
+    ctx.ws.gspo_sum = reinterpret_cast<double*>(b + L::scal + 16);
+    ctx.ws.s_seg = reinterpret_cast<double*>(b + L::scal + 24);
+    ctx.ws.seg_n = reinterpret_cast<int*>(b + L::seg_n);
+    ctx.ws.seg_dq = reinterpret_cast<unsigned long long*>(b + L::seg_dq);
+    ctx.ws.seg_absq = reinterpret_cast<unsigned long long*>(b + L::seg_absq);
+    ctx.ws.seg_nonfinite = reinterpret_cast<int*>(b + L::seg_nf);
+    ctx.ws.seg_coef = reinterpret_cast<float*>(b + L::seg_coef);
+    ctx.ws.row_counter = reinterpret_cast<int*>(b + L::counter);
+    ctx.ws.cnt_part = reinterpret_cast<long long*>(b + L::cnt_part);
+    ctx.ws.red_part = reinterpret_cast<double*>(b + L::red_part);
+    ctx.ws.done = reinterpret_cast<unsigned*>(b + L::done);
+    ctx.ws.err = reinterpret_cast<int*>(b + L::err);
+    return lmloss_forward_backward(&ctx, a, stream);
+}

@@ -85,7 +85,7 @@ def read_traffic(kernel_tag: str):
     if not os.path.exists(prof):
         return None
     h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh", "lmloss.cu"):
+    for f in ("kernels.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "lm_head_vocab_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     digest = h.hexdigest()

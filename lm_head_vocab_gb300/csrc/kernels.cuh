@@ -76,6 +76,12 @@ struct Vec<true> {
     {
         return fmaxf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
     }
+    // Pair k (elements 2k, 2k+1) of a vector as packed fp32.
+    __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
+    {
+        const uint32_t w = k == 0 ? q.x : (k == 1 ? q.y : (k == 2 ? q.z : q.w));
+        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
     __device__ static __forceinline__ float load1(const void* base, int64_t idx)
     {
         const uint16_t b = reinterpret_cast<const uint16_t*>(base)[idx];
@@ -112,6 +118,11 @@ struct Vec<false> {
         return __float_as_uint(fmaxf(m, __uint_as_float(acc)));
     }
     __device__ static __forceinline__ float max_final(uint32_t acc) { return __uint_as_float(acc); }
+    __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
+    {
+        return k == 0 ? f2_pack(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : f2_pack(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
     __device__ static __forceinline__ float load1(const void* base, int64_t idx)
     {
         return reinterpret_cast<const float*>(base)[idx];
@@ -127,99 +138,6 @@ struct Vec<false> {
 __device__ __forceinline__ float rescale(float m, float M)
 {
     return (m == M) ? 1.0f : ex2((m - M) * kLog2e);
-}
-
-struct Part {
-    float m, s;      // non-target max and sum
-    float mu, su, w; // teacher max and sum, sum e^(u-mu) (u - z)
-    float zt;        // target logit (valid iff has_t)
-    int has_t;
-};
-
-__device__ __forceinline__ Part part_empty()
-{
-    Part p;
-    p.m = -INFINITY; p.s = 0.f; p.mu = -INFINITY; p.su = 0.f; p.w = 0.f; p.zt = 0.f; p.has_t = 0;
-    return p;
-}
-
-template <bool KL>
-__device__ __forceinline__ void part_merge(Part& a, const Part& b)
-{
-    const float M = fmaxf(a.m, b.m);
-    a.s = a.s * rescale(a.m, M) + b.s * rescale(b.m, M);
-    a.m = M;
-    if (KL) {
-        const float Mu = fmaxf(a.mu, b.mu);
-        const float fa = rescale(a.mu, Mu), fb = rescale(b.mu, Mu);
-        a.su = a.su * fa + b.su * fb;
-        a.w = a.w * fa + b.w * fb;
-        a.mu = Mu;
-    }
-    if (b.has_t && !a.has_t) { a.zt = b.zt; a.has_t = 1; }
-}
-
-template <bool KL>
-__device__ __forceinline__ Part part_shfl_xor(const Part& p, int mask)
-{
-    Part q;
-    q.m = __shfl_xor_sync(0xffffffffu, p.m, mask);
-    q.s = __shfl_xor_sync(0xffffffffu, p.s, mask);
-    if (KL) {
-        q.mu = __shfl_xor_sync(0xffffffffu, p.mu, mask);
-        q.su = __shfl_xor_sync(0xffffffffu, p.su, mask);
-        q.w = __shfl_xor_sync(0xffffffffu, p.w, mask);
-    } else {
-        q.mu = -INFINITY; q.su = 0.f; q.w = 0.f;
-    }
-    q.zt = __shfl_xor_sync(0xffffffffu, p.zt, mask);
-    q.has_t = __shfl_xor_sync(0xffffffffu, p.has_t, mask);
-    return q;
-}
-
-// Butterfly over a warp; every lane ends with the same merged value.
-// Merge order is fixed by lane index, so results are reproducible bit for bit.
-template <bool KL>
-__device__ __forceinline__ Part warp_merge(Part p)
-{
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        Part q = part_shfl_xor<KL>(p, off);
-        // lower lane always acts as "a" so both partners compute the same value
-        if (threadIdx.x & off) { Part t = q; part_merge<KL>(t, p); p = t; }
-        else part_merge<KL>(p, q);
-    }
-    return p;
-}
-
-// Per-row scalars shared by every kernel.
-struct RowScalars {
-    float nll, lse, p_t, tg;        // tg = d CE / d z_t (p_t - 1 or -p_nt)
-    float lse_u, kl;                // teacher
-};
-
-// From the row's merged partial: the collapse-free NLL and its companions.
-template <bool KL>
-__device__ __forceinline__ RowScalars row_scalars(const Part& P, bool bad_target)
-{
-    RowScalars r;
-    const float zt = bad_target ? __int_as_float(0x7fc00000) : P.zt;
-    const float lse_nt = (P.s == 0.f) ? -INFINITY : P.m + logf(P.s);
-    const float d = lse_nt - zt;
-    r.nll = (d > 0.f) ? d + log1pf(expf(-d)) : log1pf(expf(d));
-    r.lse = fmaxf(zt, lse_nt) + log1pf(expf(-fabsf(d)));
-    if (isnan(d)) r.lse = d;
-    r.p_t = expf(-r.nll);
-    const float p_nt = -expm1f(-r.nll);
-    r.tg = (r.p_t < 0.25f) ? r.p_t - 1.0f : -p_nt;
-    if (KL) {
-        r.lse_u = P.mu + logf(P.su);
-        r.kl = P.w / P.su - (r.lse_u - r.lse);
-    } else {
-        r.lse_u = 0.f;
-        r.kl = 0.f;
-    }
-    return r;
 }
 
 // ------------------------------------------------------------ parameters
@@ -244,6 +162,11 @@ struct Workspace {
 };
 
 constexpr int kRedBlocks = 64;   // blocks of the count and reduce kernels
+
+// Modes of the staged-row kernel: statistics and gradient in one pass; the
+// statistics alone (forward only, and the first pass of GSPO); the gradient
+// alone from statistics already in the workspace (GSPO's pass after its seam).
+enum : int { kModeFused = 0, kModeStats = 1, kModeGrad = 2 };
 
 struct CallParams {
     const void* logits;
@@ -270,7 +193,8 @@ struct CallParams {
     uint8_t* seg_flag_out;
     float* seg_loss_out;
     Workspace ws;
-    // fused-kernel launch shape
+    // fused-kernel launch shape and mode
+    int mode;               // kModeFused, kModeStats or kModeGrad
     int cluster;
     int64_t slice;          // elements per CTA of a row (multiple of the vector width)
     int nbuf;
@@ -443,6 +367,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
     const int64_t c1 = min(p.V, c0 + p.slice);
     const int nbuf = p.nbuf;
     const float s_tok = token_scale(p);
+    const int mode = p.mode;
 
     auto buf_addr = [&](int b, int a) -> uint32_t {
         return smem_addr(bufs + (static_cast<size_t>(b) * (KL ? 2 : 1) + a) * p.buf_bytes);
@@ -507,26 +432,38 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
         const uint32_t bu = KL ? buf_addr(b, 1) : 0u;
         const int64_t tv = t - e0;   // target offset within the interior (may be outside)
         const bool owner = act && t >= c0 && t < c1;
+        // the one interior vector holding the target (-1 if none) and its lane
+        const int vt = (act && tv >= 0 && tv < static_cast<int64_t>(nvec) * VN) ? static_cast<int>(tv / VN) : -1;
+        const int kt = (vt >= 0) ? static_cast<int>(tv - static_cast<int64_t>(vt) * VN) : -1;
 
         if (!failed && !mbar_wait_bounded(bar_addr(b), parity, kWaitLimitCycles)) {
             set_error(p.ws.err, kErrTimeout);
             failed = true;
         }
 
+        // GSPO gradient pass: the row's statistics and segment coefficient come
+        // from the workspace; start those loads now, they are needed after the wait
+        float g_lse = 0.f, g_nll = 0.f, g_cr = 0.f;
+        if (mode == kModeGrad && warp == 0 && lane == 0 && act && !bad) {
+            g_lse = p.ws.row_lse[r];
+            g_nll = p.ws.row_nll[r];
+            const int gs = p.seg_ids ? p.seg_ids[r] : -1;
+            g_cr = (gs >= 0 && gs < p.num_segments) ? p.ws.seg_coef[gs] : 0.f;
+        }
+
         // ---- pass A: maxima (non-target for z, all columns for u)
-        if (act) {
+        if (act && mode != kModeGrad) {
             uint32_t accz = IO::max_init(), accu = IO::max_init();
             float mx = -INFINITY, mu = -INFINITY;
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
-                const int64_t k = tv - static_cast<int64_t>(v) * VN;
-                if (k >= 0 && k < VN) {
+                if (v == vt) {
                     float x[VN];
                     IO::unpack(q, x);
 #pragma unroll
                     for (int j = 0; j < VN; ++j) {
-                        if (j != k) mx = fmaxf(mx, x[j]);
+                        if (j != kt) mx = fmaxf(mx, x[j]);
                         else slot[0] = x[j];
                     }
                 } else {
@@ -562,7 +499,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 
         // ---- pass B: sums relative to the CTA maximum
         float m_cta = -INFINITY, mu_cta = -INFINITY;
-        if (act) {
+        if (act && mode != kModeGrad) {
             m_cta = (lane < NW) ? wred[lane] : -INFINITY;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
@@ -575,6 +512,35 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
             const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
             float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f;
+            if (!KL) {
+                // packed pairs: one f32x2 FMA forms two exponent arguments, one
+                // f32x2 add accumulates two terms
+                const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                const uint64_t nm2 = f2_pack(-mL, -mL);
+                uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    const uint4 q = lds128(bz + v * 16);
+                    if (v != vt) {
+#pragma unroll
+                        for (int k = 0; k < VN / 2; ++k) {
+                            float a0, a1;
+                            f2_unpack(f2_fma(IO::pair(q, k), L2, nm2), a0, a1);
+                            acc = f2_add(acc, f2_pack(ex2(a0), ex2(a1)));
+                        }
+                    } else {
+                        float x[VN];
+                        IO::unpack(q, x);
+#pragma unroll
+                        for (int j = 0; j < VN; ++j)
+                            if (j != kt) s0 += ex2(fmaf(x[j], kLog2e, -mL));
+                    }
+                }
+                float h0, h1;
+                f2_unpack(acc, h0, h1);
+                s1 = h0 + h1;
+            }
+            if (KL) {
 #pragma unroll 2
             for (int v = tid; v < nvec; v += NT) {
                 float x[VN];
@@ -582,15 +548,14 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 float e[VN];
 #pragma unroll
                 for (int j = 0; j < VN; ++j) e[j] = ex2(fmaf(x[j], kLog2e, -mL));
-                const int64_t k = tv - static_cast<int64_t>(v) * VN;
-                if (k >= 0 && k < VN) {
+                if (v == vt) {
 #pragma unroll
                     for (int j = 0; j < VN; ++j)
-                        if (j == k) e[j] = 0.f;
+                        if (j == kt) e[j] = 0.f;
                 }
 #pragma unroll
                 for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
-                if (KL) {
+                {
                     float y[VN];
                     IO::unpack(lds128(bu + v * 16), y);
 #pragma unroll
@@ -600,6 +565,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                         w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
                     }
                 }
+            }
             }
             float s = s0 + s1;
             if (tid == NT - 1) {
@@ -692,7 +658,30 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
-            if (act) {
+            if (act && mode == kModeGrad) {
+                if (lane == 0) {
+                    // s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot)
+                    const float nll = bad ? __int_as_float(0x7fc00000) : g_nll;
+                    const float lse = bad ? nll : g_lse;
+                    const float pt = expf(-nll);
+                    const float tg = (pt < 0.25f) ? pt - 1.0f : expm1f(-nll);
+                    const float s = s_tok;
+                    const float zc = 2.f * p.alpha * lse;
+                    const float a = s * (p.w_ce + zc) + g_cr;
+                    RowCoef cf;
+                    const float lseL = lse * kLog2e;
+                    const float lseL_err = fmaf(lse, kLog2e, -lseL);
+                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2f(fabsf(a)));
+                    cf.neg = a < 0.f;
+                    cf.lseL = lseL;
+                    cf.luL = 0.f;
+                    cf.a = a;
+                    cf.b = 0.f;
+                    cf.gt = (s * p.w_ce + g_cr) * tg + s * zc * pt;
+                    cf.pad = 0;
+                    *coef = cf;
+                }
+            } else if (act) {
                 float M = q.m;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -760,7 +749,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                         if (p.kl_out) p.kl_out[r] = kl;
                     }
                 }
-            } else if (lane == 0 && rank == 0) {
+            } else if (lane == 0 && rank == 0 && mode != kModeGrad) {
                 p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f;
                 if (p.logp_out) p.logp_out[r] = 0.f;
                 if (p.lse_out) p.lse_out[r] = 0.f;
@@ -774,7 +763,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
         __syncthreads();
 
         // ---- pass C: gradient of the slice, written once
-        if (p.grad) {
+        if (p.grad && mode != kModeStats) {
             unsigned char* g = static_cast<unsigned char*>(p.grad) + row_off + static_cast<size_t>(e0) * ESZ;
             if (!act) {
                 for (int v = tid; v < nvec; v += NT) stg128(g + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
@@ -796,30 +785,37 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                         qv[j] = cf.b * ex2(fmaf(y[j], kLog2e, -cf.luL));
                         gv[j] = fmaf(cf.a, ex2(fmaf(x[j], kLog2e, -cf.lseL)), -qv[j]);
                     }
-                    const int64_t k = tv - static_cast<int64_t>(v) * VN;
-                    if (k >= 0 && k < VN) {
+                    if (v == vt) {
 #pragma unroll
                         for (int j = 0; j < VN; ++j)
-                            if (j == k) gv[j] = cf.gt - qv[j];
+                            if (j == kt) gv[j] = cf.gt - qv[j];
                     }
                     stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                 }
             } else {
                 auto body = [&](auto NEG) {
+                    // g_j = (+-) 2^(z_j log2e - cz), two arguments per f32x2 FMA
+                    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                    const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
 #pragma unroll 2
                     for (int v = tid; v < nvec; v += NT) {
-                        float x[VN], gv[VN];
-                        IO::unpack(lds128(bz + v * 16), x);
+                        const uint4 q = lds128(bz + v * 16);
+                        float gv[VN];
 #pragma unroll
-                        for (int j = 0; j < VN; ++j) {
-                            const float e = ex2(fmaf(x[j], kLog2e, -cf.cz));
-                            gv[j] = decltype(NEG)::value ? -e : e;
+                        for (int k = 0; k < VN / 2; ++k) {
+                            float a0, a1;
+                            f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
+                            gv[2 * k] = ex2(a0);
+                            gv[2 * k + 1] = ex2(a1);
                         }
-                        const int64_t k = tv - static_cast<int64_t>(v) * VN;
-                        if (k >= 0 && k < VN) {
+                        if (decltype(NEG)::value) {
+#pragma unroll
+                            for (int j = 0; j < VN; ++j) gv[j] = -gv[j];
+                        }
+                        if (v == vt) {
 #pragma unroll
                             for (int j = 0; j < VN; ++j)
-                                if (j == k) gv[j] = cf.gt;
+                                if (j == kt) gv[j] = cf.gt;
                         }
                         stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                     }
@@ -847,129 +843,6 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
         }
     }
     cluster_sync_all();   // no CTA leaves while a peer may still read its records
-}
-
-// ======================================================================
-// Streaming statistics kernel (forward only, and phase 1 of GSPO): one CTA
-// per row at a time, online max/sum in registers, no staging.
-// ======================================================================
-template <bool BF16, bool KL, int NT>
-__global__ void __launch_bounds__(NT, 2) stats_kernel(const CallParams p)
-{
-    using IO = Vec<BF16>;
-    constexpr int VN = IO::N;
-    constexpr int ESZ = IO::ESZ;
-    constexpr int NW = NT / 32;
-    __shared__ Part wpart[NW];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    for (int64_t r = blockIdx.x; r < p.T; r += gridDim.x) {
-        int64_t t;
-        const bool act = row_active(p, r, t);
-        if (!act) {
-            if (tid == 0) {
-                p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f;
-                if (p.logp_out) p.logp_out[r] = 0.f;
-                if (p.lse_out) p.lse_out[r] = 0.f;
-                if (p.kl_out) p.kl_out[r] = 0.f;
-            }
-            continue;
-        }
-        const bool bad = (t < 0 || t >= p.V);
-        int64_t e0, e1;
-        row_interior<ESZ>(p.logits, r, p.ld, 0, p.V, e0, e1);
-        const int nvec = static_cast<int>((e1 - e0) / VN);
-        const unsigned char* zrow = static_cast<const unsigned char*>(p.logits) + static_cast<size_t>(r * p.ld + e0) * ESZ;
-        const unsigned char* urow = KL ? static_cast<const unsigned char*>(p.teacher) + static_cast<size_t>(r * p.ld + e0) * ESZ : nullptr;
-        const int64_t tv = t - e0;
-
-        Part P = part_empty();
-        auto add_z = [&](const float (&x)[VN], int64_t k) {
-            float vm = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < VN; ++j)
-                if (j != k) vm = fmaxf(vm, x[j]);
-            if (vm > P.m) { P.s *= rescale(P.m, vm); P.m = vm; }
-            const float mL = (P.m == -INFINITY) ? 0.f : P.m * kLog2e;
-#pragma unroll
-            for (int j = 0; j < VN; ++j) {
-                if (j == k) { P.zt = x[j]; P.has_t = 1; }
-                else P.s += ex2(fmaf(x[j], kLog2e, -mL));
-            }
-        };
-        auto add_u = [&](const float (&x)[VN], const float (&y)[VN]) {
-            float vm = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < VN; ++j) vm = fmaxf(vm, y[j]);
-            if (vm > P.mu) { const float f = rescale(P.mu, vm); P.su *= f; P.w *= f; P.mu = vm; }
-            const float muL = (P.mu == -INFINITY) ? 0.f : P.mu * kLog2e;
-#pragma unroll
-            for (int j = 0; j < VN; ++j) {
-                const float eu = ex2(fmaf(y[j], kLog2e, -muL));
-                P.su += eu;
-                P.w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
-            }
-        };
-        // four independent 16-byte loads in flight per thread before any arithmetic
-        constexpr int U = 4;
-        for (int v0 = tid; v0 < nvec; v0 += U * NT) {
-            uint4 qz[U], qu[U];
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int v = v0 + k * NT;
-                if (v < nvec) {
-                    qz[k] = ldg_stream(zrow + static_cast<size_t>(v) * 16);
-                    if (KL) qu[k] = ldg_stream(urow + static_cast<size_t>(v) * 16);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int v = v0 + k * NT;
-                if (v >= nvec) break;
-                float x[VN];
-                IO::unpack(qz[k], x);
-                const int64_t kk = tv - static_cast<int64_t>(v) * VN;
-                add_z(x, (kk >= 0 && kk < VN) ? kk : -1);
-                if (KL) {
-                    float y[VN];
-                    IO::unpack(qu[k], y);
-                    add_u(x, y);
-                }
-            }
-        }
-        if (tid == NT - 1) {
-            for (int pass = 0; pass < 2; ++pass) {
-                const int64_t lo = pass == 0 ? 0 : e1, hi = pass == 0 ? e0 : p.V;
-                for (int64_t j = lo; j < hi; ++j) {
-                    float x[VN], y[VN];
-                    for (int q = 0; q < VN; ++q) { x[q] = -INFINITY; y[q] = -INFINITY; }
-                    x[0] = IO::load1(p.logits, r * p.ld + j);
-                    add_z(x, j == t ? 0 : -1);
-                    if (KL) {
-                        y[0] = IO::load1(p.teacher, r * p.ld + j);
-                        add_u(x, y);
-                    }
-                }
-            }
-        }
-        P = warp_merge<KL>(P);
-        if (lane == 0) wpart[warp] = P;
-        __syncthreads();
-        if (warp == 0) {
-            Part q = (lane < NW) ? wpart[lane] : part_empty();
-            q = warp_merge<KL>(q);
-            if (lane == 0) {
-                const RowScalars S = row_scalars<KL>(q, bad);
-                p.ws.row_nll[r] = S.nll;
-                p.ws.row_lse[r] = S.lse;
-                p.ws.row_kl[r] = S.kl;
-                if (p.logp_out) p.logp_out[r] = -S.nll;
-                if (p.lse_out) p.lse_out[r] = S.lse;
-                if (p.kl_out) p.kl_out[r] = S.kl;
-            }
-        }
-        __syncthreads();
-    }
 }
 
 // ======================================================================
@@ -1020,6 +893,7 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
         long long tot = 0;
         for (int k = 0; k < nw; ++k) tot += ipart[k];
         *p.ws.n_nonempty = tot;
+        *p.ws.row_counter = 0;   // the gradient pass hands out rows afresh
         s_seg_sh = (p.reduction == 1) ? (tot > 0 ? 1.0 / static_cast<double>(tot) : 0.0) : p.inv_denominator;
         *p.ws.s_seg = s_seg_sh;
     }
@@ -1065,85 +939,6 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
         double tot = 0.0;
         for (int k = 0; k < nw; ++k) tot += dpart[k];
         *p.ws.gspo_sum = tot;
-    }
-}
-
-// ======================================================================
-// Streaming gradient kernel (GSPO phase 3): re-reads the logits and writes
-// s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot) once per element.
-// ======================================================================
-template <bool BF16, int NT>
-__global__ void __launch_bounds__(NT, 2) grad_kernel(const CallParams p)
-{
-    using IO = Vec<BF16>;
-    constexpr int VN = IO::N;
-    constexpr int ESZ = IO::ESZ;
-    const int tid = threadIdx.x;
-    const float s_tok = token_scale(p);
-
-    for (int64_t r = blockIdx.x; r < p.T; r += gridDim.x) {
-        int64_t t;
-        const bool act = row_active(p, r, t);
-        int64_t e0, e1;
-        row_interior<ESZ>(p.logits, r, p.ld, 0, p.V, e0, e1);
-        const int nvec = static_cast<int>((e1 - e0) / VN);
-        const size_t off = static_cast<size_t>(r * p.ld + e0) * ESZ;
-        const unsigned char* zrow = static_cast<const unsigned char*>(p.logits) + off;
-        unsigned char* grow = static_cast<unsigned char*>(p.grad) + off;
-        if (!act) {
-            for (int v = tid; v < nvec; v += NT) stg128(grow + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
-            if (tid == NT - 1) {
-                for (int64_t j = 0; j < e0; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
-                for (int64_t j = e1; j < p.V; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
-            }
-            continue;
-        }
-        const float nll = p.ws.row_nll[r];
-        const float lse = p.ws.row_lse[r];
-        const int g = p.seg_ids ? p.seg_ids[r] : -1;
-        const float c_r = (g >= 0 && g < p.num_segments) ? p.ws.seg_coef[g] : 0.f;
-        const float p_t = expf(-nll);
-        const float p_nt = -expm1f(-nll);
-        const float tg = (p_t < 0.25f) ? p_t - 1.0f : -p_nt;
-        const float zcoef = 2.f * p.alpha * lse;
-        const float a = s_tok * (p.w_ce + zcoef) + c_r;
-        const float gt = (s_tok * p.w_ce + c_r) * tg + s_tok * zcoef * p_t;
-        const float lseL = lse * kLog2e;
-        const int64_t tv = t - e0;
-        constexpr int U = 4;
-        for (int v0 = tid; v0 < nvec; v0 += U * NT) {
-            uint4 qz[U];
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int v = v0 + k * NT;
-                if (v < nvec) qz[k] = ldg_stream(zrow + static_cast<size_t>(v) * 16);
-            }
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int v = v0 + k * NT;
-                if (v >= nvec) break;
-                float x[VN], gv[VN];
-                IO::unpack(qz[k], x);
-#pragma unroll
-                for (int j = 0; j < VN; ++j) gv[j] = a * ex2(fmaf(x[j], kLog2e, -lseL));
-                const int64_t kk = tv - static_cast<int64_t>(v) * VN;
-                if (kk >= 0 && kk < VN) {
-#pragma unroll
-                    for (int j = 0; j < VN; ++j)
-                        if (j == kk) gv[j] = gt;
-                }
-                stg128(grow + static_cast<size_t>(v) * 16, IO::pack(gv));
-            }
-        }
-        if (tid == NT - 1) {
-            for (int pass = 0; pass < 2; ++pass) {
-                const int64_t lo = pass == 0 ? 0 : e1, hi = pass == 0 ? e0 : p.V;
-                for (int64_t j = lo; j < hi; ++j) {
-                    const float x = IO::load1(p.logits, r * p.ld + j);
-                    IO::store1(p.grad, r * p.ld + j, (j == t) ? gt : a * ex2(fmaf(x, kLog2e, -lseL)));
-                }
-            }
-        }
     }
 }
 

@@ -184,20 +184,47 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
     return LMLOSS_OK;
 }
 
-template <typename K>
-int resident_grid(K kernel, int threads, int num_sms, int64_t rows)
-{
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    int64_t g = static_cast<int64_t>(per_sm) * num_sms;
-    if (rows < g) g = rows;
-    return static_cast<int>(g < 1 ? 1 : g);
-}
-
 lmloss_status launch_err()
 {
     return cudaGetLastError() == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
+}
+
+// Plan and launch the staged-row kernel in one of its modes.
+lmloss_status launch_fused(lmloss_ctx* h, const lmloss_args* a, CallParams& p, int mode, cudaStream_t stream,
+                           lmloss_call_info& info)
+{
+    FusedPlan P;
+    lmloss_status st = plan_fused(h, a, P);
+    if (st != LMLOSS_OK) return st;
+    p.mode = mode;
+    p.cluster = P.C;
+    p.slice = P.slice;
+    p.nbuf = P.nbuf;
+    p.buf_bytes = P.buf_bytes;
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(P.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(P.NT));
+    cfg.dynamicSmemBytes = P.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* kargs[] = {&p};
+    if (cudaLaunchKernelExC(&cfg, P.fn, kargs) != cudaSuccess) {
+        cudaGetLastError();
+        return LMLOSS_ERR_CUDA;
+    }
+    info.launches += 1;
+    info.cluster = P.C;
+    info.threads = P.NT;
+    info.nbuf = P.nbuf;
+    info.grid = P.grid;
+    info.smem_bytes = static_cast<int32_t>(P.smem);
+    return LMLOSS_OK;
 }
 
 }  // namespace
@@ -357,7 +384,6 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     DeviceGuard g(h->device);
     if (!g.ok) return LMLOSS_ERR_CUDA;
 
-    const bool bf16 = a->dtype == LMLOSS_BF16;
     const bool kl = a->teacher_logits != nullptr;
     const bool gspo = a->segment_ids != nullptr;
 
@@ -393,7 +419,6 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     p.ws = h->ws;
 
     lmloss_call_info info{};
-    const int NT_STREAM = 512;
 
     // count / reduce: one block per 64 rows, at most kRedBlocks, at least one
     int64_t rb = (a->T + 63) / 64;
@@ -416,55 +441,13 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     }
     if (a->T > 0) {
         if (!gspo && a->grad_out) {
-            FusedPlan P;
-            if ((st = plan_fused(h, a, P)) != LMLOSS_OK) return st;
-            p.cluster = P.C;
-            p.slice = P.slice;
-            p.nbuf = P.nbuf;
-            p.buf_bytes = P.buf_bytes;
-            cudaLaunchConfig_t cfg{};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = P.C;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(static_cast<unsigned>(P.grid));
-            cfg.blockDim = dim3(static_cast<unsigned>(P.NT));
-            cfg.dynamicSmemBytes = P.smem;
-            cfg.stream = stream;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            void* kargs[] = {&p};
-            if (cudaLaunchKernelExC(&cfg, P.fn, kargs) != cudaSuccess) {
-                cudaGetLastError();
-                return LMLOSS_ERR_CUDA;
-            }
-            info.launches += 1;
+            // one read of the logits, one write of the gradient
+            if ((st = launch_fused(h, a, p, kModeFused, stream, info)) != LMLOSS_OK) return st;
             info.path = 0;
-            info.cluster = P.C;
-            info.threads = P.NT;
-            info.nbuf = P.nbuf;
-            info.grid = P.grid;
-            info.smem_bytes = static_cast<int32_t>(P.smem);
         } else {
-            int grid;
-            if (bf16) {
-                if (kl) { grid = resident_grid(stats_kernel<true, true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                          stats_kernel<true, true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
-                else    { grid = resident_grid(stats_kernel<true, false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                          stats_kernel<true, false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
-            } else {
-                if (kl) { grid = resident_grid(stats_kernel<false, true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                          stats_kernel<false, true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
-                else    { grid = resident_grid(stats_kernel<false, false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                          stats_kernel<false, false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p); }
-            }
-            if ((st = launch_err()) != LMLOSS_OK) return st;
-            info.launches += 1;
+            // statistics pass (forward only, or the first pass of GSPO)
+            if ((st = launch_fused(h, a, p, kModeStats, stream, info)) != LMLOSS_OK) return st;
             info.path = gspo ? 2 : 1;
-            info.cluster = 1;
-            info.threads = NT_STREAM;
-            info.grid = grid;
             if (gspo) {
                 const int tg = 256;
                 int64_t gb = (a->T + tg - 1) / tg;
@@ -474,17 +457,8 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
                 seam_finish_kernel<<<1, 1024, 0, stream>>>(p);
                 if ((st = launch_err()) != LMLOSS_OK) return st;
                 info.launches += 2;
-                if (a->grad_out) {
-                    if (bf16) {
-                        grid = resident_grid(grad_kernel<true, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                        grad_kernel<true, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p);
-                    } else {
-                        grid = resident_grid(grad_kernel<false, NT_STREAM>, NT_STREAM, h->num_sms, a->T);
-                        grad_kernel<false, NT_STREAM><<<grid, NT_STREAM, 0, stream>>>(p);
-                    }
-                    if ((st = launch_err()) != LMLOSS_OK) return st;
-                    info.launches += 1;
-                }
+                // the seam has seen every row: the gradient pass reads the logits again
+                if (a->grad_out && (st = launch_fused(h, a, p, kModeGrad, stream, info)) != LMLOSS_OK) return st;
             }
         }
     }

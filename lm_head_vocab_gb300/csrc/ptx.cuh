@@ -124,20 +124,6 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank)
     return remote;
 }
 
-__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // ---------------------------------------------------------------- memory
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -148,21 +134,39 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
-// Streaming 16-byte global load that does not allocate in L1.  Not the
-// non-coherent path: the gradient may overwrite the logits in place.
-__device__ __forceinline__ uint4 ldg_stream(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ void stg128(void* p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// ------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register: Blackwell's f32x2 instructions do
+// both lanes' FMA / add in one issue slot.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // ---------------------------------------------------------------- math

@@ -179,6 +179,13 @@ lmloss_status lmloss_set_launch_config(lmloss_handle handle, int cluster, int th
 lmloss_status lmloss_set_timing(lmloss_handle handle, int enable);
 lmloss_status lmloss_get_timing(lmloss_handle handle, float* total_ms, int32_t* calls);
 
+/* Failure-detection self-test (diagnostic; synchronises the device): runs the
+ * bounded wait that guards every copy in the kernels on a barrier that nothing
+ * arrives at, giving up after limit_cycles SM clock cycles.  Returns
+ * LMLOSS_ERR_TIMEOUT when the wait gave up as it should (LMLOSS_OK if it
+ * somehow completed), with the device still usable. */
+lmloss_status lmloss_selftest_bounded_wait(lmloss_handle handle, long long limit_cycles);
+
 /* Launch shape and kernel count of the last call on this handle. */
 lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info);
 

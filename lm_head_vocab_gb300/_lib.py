@@ -120,6 +120,7 @@ def load() -> ctypes.CDLL:
         "lmloss_set_timing": ([h, ctypes.c_int], st),
         "lmloss_get_timing": ([h, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)], st),
         "lmloss_get_call_info": ([h, ctypes.POINTER(lmloss_call_info)], st),
+        "lmloss_selftest_bounded_wait": ([h, ctypes.c_longlong], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -188,6 +189,10 @@ def lmloss_get_timing(handle):
     if st != LMLOSS_OK:
         raise LMLossError(st, "lmloss_get_timing")
     return float(ms.value), int(n.value)
+
+
+def lmloss_selftest_bounded_wait(handle, limit_cycles: int) -> int:
+    return load().lmloss_selftest_bounded_wait(handle, int(limit_cycles))
 
 
 def lmloss_get_call_info(handle) -> dict:

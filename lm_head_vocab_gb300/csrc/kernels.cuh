@@ -76,6 +76,22 @@ struct Vec<true> {
     {
         return fmaxf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
     }
+    // Running packed minimum (used to spot -inf teacher logits).
+    __device__ static __forceinline__ uint32_t min_init() { return 0x7f807f80u; }  // (+inf, +inf)
+    __device__ static __forceinline__ uint32_t min_acc(uint32_t acc, const uint4& q)
+    {
+        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
+        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&q.z);
+        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&q.w);
+        __nv_bfloat162 m = __hmin2(__hmin2(a, b), __hmin2(c, d));
+        __nv_bfloat162 r = __hmin2(m, *reinterpret_cast<__nv_bfloat162*>(&acc));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+    __device__ static __forceinline__ float min_final(uint32_t acc)
+    {
+        return fminf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
+    }
     // Pair k (elements 2k, 2k+1) of a vector as packed fp32.
     __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
     {
@@ -118,6 +134,14 @@ struct Vec<false> {
         return __float_as_uint(fmaxf(m, __uint_as_float(acc)));
     }
     __device__ static __forceinline__ float max_final(uint32_t acc) { return __uint_as_float(acc); }
+    __device__ static __forceinline__ uint32_t min_init() { return 0x7f800000u; }
+    __device__ static __forceinline__ uint32_t min_acc(uint32_t acc, const uint4& q)
+    {
+        float m = fminf(fminf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                        fminf(__uint_as_float(q.z), __uint_as_float(q.w)));
+        return __float_as_uint(fminf(m, __uint_as_float(acc)));
+    }
+    __device__ static __forceinline__ float min_final(uint32_t acc) { return __uint_as_float(acc); }
     __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
     {
         return k == 0 ? f2_pack(__uint_as_float(q.x), __uint_as_float(q.y))
@@ -329,12 +353,12 @@ struct ClusterRec {     // one CTA's partial for the current row (32 bytes)
 static_assert(sizeof(ClusterRec) == 32, "record is two 16-byte pushes");
 
 struct RowCoef {        // the row's gradient coefficients, shared by the CTA's threads
-    float cz;           // non-teacher: g_j = sign * 2^(z_j log2e - cz)
+    float cz;           // a p_j = sign(a) 2^(z_j log2e - cz)
+    float cq;           // teacher: b q_j = 2^(u_j log2e - cq) when b > 0
     float lseL, luL;    // teacher: p_j = 2^(z_j log2e - lseL), q_j = 2^(u_j log2e - luL)
     float a, b;         // teacher: g_j = a p_j - b q_j
     float gt;           // target column (teacher: minus b q_t still to apply)
     int neg;            // sign of a
-    int pad;
 };
 
 template <bool BF16, bool KL, int NT>
@@ -353,7 +377,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
     int* tq = reinterpret_cast<int*>(smem + 48);                         // [4] its target (-100: inactive)
     float* slot = reinterpret_cast<float*>(smem + 64);                   // [1] target logit
     RowCoef* coef = reinterpret_cast<RowCoef*>(smem + 96);               // [1]
-    float* wred = reinterpret_cast<float*>(smem + 256);                  // [5][32]
+    float* wred = reinterpret_cast<float*>(smem + 256);                  // [6][32]
     ClusterRec* rec = reinterpret_cast<ClusterRec*>(smem + 1024);        // [2][kMaxCluster]
     unsigned char* bufs = smem + kHdrBytes;
 
@@ -453,8 +477,8 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 
         // ---- pass A: maxima (non-target for z, all columns for u)
         if (act && mode != kModeGrad) {
-            uint32_t accz = IO::max_init(), accu = IO::max_init();
-            float mx = -INFINITY, mu = -INFINITY;
+            uint32_t accz = IO::max_init(), accu = IO::max_init(), accn = IO::min_init();
+            float mx = -INFINITY, mu = -INFINITY, un = INFINITY;
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
@@ -469,7 +493,11 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 } else {
                     accz = IO::max_acc(accz, q);
                 }
-                if (KL) accu = IO::max_acc(accu, lds128(bu + v * 16));
+                if (KL) {
+                    const uint4 qu = lds128(bu + v * 16);
+                    accu = IO::max_acc(accu, qu);
+                    accn = IO::min_acc(accn, qu);
+                }
             }
             if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
@@ -478,7 +506,11 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                         const float x = IO::load1(p.logits, r * p.ld + j);
                         if (j != t) mx = fmaxf(mx, x);
                         else slot[0] = x;
-                        if (KL) mu = fmaxf(mu, IO::load1(p.teacher, r * p.ld + j));
+                        if (KL) {
+                            const float y = IO::load1(p.teacher, r * p.ld + j);
+                            mu = fmaxf(mu, y);
+                            un = fminf(un, y);
+                        }
                     }
                 }
             }
@@ -487,12 +519,16 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
             if (KL) {
                 mu = fmaxf(mu, IO::max_final(accu));
+                un = fminf(un, IO::min_final(accn));
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+                for (int off = 16; off > 0; off >>= 1) {
+                    mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+                    un = fminf(un, __shfl_xor_sync(0xffffffffu, un, off));
+                }
             }
             if (lane == 0) {
                 wred[warp] = m;
-                if (KL) wred[32 + warp] = mu;
+                if (KL) { wred[32 + warp] = mu; wred[160 + warp] = un; }
             }
         }
         __syncthreads();
@@ -541,31 +577,69 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 s1 = h0 + h1;
             }
             if (KL) {
+                // with no -inf teacher logit in the slice, e^(u-mu) (u - z) needs no guard
+                float un_cta = (lane < NW) ? wred[160 + lane] : INFINITY;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) un_cta = fminf(un_cta, __shfl_xor_sync(0xffffffffu, un_cta, off));
+                if (un_cta > -INFINITY) {
+                    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                    const uint64_t nm2 = f2_pack(-mL, -mL);
+                    const uint64_t nmu2 = f2_pack(-muL, -muL);
+                    const uint64_t neg1 = f2_pack(-1.f, -1.f);
+                    uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz;
 #pragma unroll 2
-            for (int v = tid; v < nvec; v += NT) {
-                float x[VN];
-                IO::unpack(lds128(bz + v * 16), x);
-                float e[VN];
+                    for (int v = tid; v < nvec; v += NT) {
+                        const uint4 q = lds128(bz + v * 16);
+                        const uint4 qu = lds128(bu + v * 16);
 #pragma unroll
-                for (int j = 0; j < VN; ++j) e[j] = ex2(fmaf(x[j], kLog2e, -mL));
-                if (v == vt) {
+                        for (int k = 0; k < VN / 2; ++k) {
+                            const uint64_t xz = IO::pair(q, k), xu = IO::pair(qu, k);
+                            float a0, a1, b0, b1;
+                            f2_unpack(f2_fma(xz, L2, nm2), a0, a1);
+                            f2_unpack(f2_fma(xu, L2, nmu2), b0, b1);
+                            float e0 = ex2(a0), e1 = ex2(a1);
+                            if (v == vt) {
+                                if (2 * k == kt) e0 = 0.f;
+                                if (2 * k + 1 == kt) e1 = 0.f;
+                            }
+                            accz = f2_add(accz, f2_pack(e0, e1));
+                            const uint64_t eu = f2_pack(ex2(b0), ex2(b1));
+                            accu = f2_add(accu, eu);
+                            accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
+                        }
+                    }
+                    float h0, h1;
+                    f2_unpack(accz, h0, h1);
+                    s0 = h0 + h1;
+                    f2_unpack(accu, h0, h1);
+                    su = h0 + h1;
+                    f2_unpack(accw, h0, h1);
+                    w = h0 + h1;
+                } else {
+#pragma unroll 2
+                    for (int v = tid; v < nvec; v += NT) {
+                        float x[VN];
+                        IO::unpack(lds128(bz + v * 16), x);
+                        float e[VN];
 #pragma unroll
-                    for (int j = 0; j < VN; ++j)
-                        if (j == kt) e[j] = 0.f;
-                }
+                        for (int j = 0; j < VN; ++j) e[j] = ex2(fmaf(x[j], kLog2e, -mL));
+                        if (v == vt) {
 #pragma unroll
-                for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
-                {
-                    float y[VN];
-                    IO::unpack(lds128(bu + v * 16), y);
+                            for (int j = 0; j < VN; ++j)
+                                if (j == kt) e[j] = 0.f;
+                        }
 #pragma unroll
-                    for (int j = 0; j < VN; ++j) {
-                        const float eu = ex2(fmaf(y[j], kLog2e, -muL));
-                        su += eu;
-                        w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
+                        for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
+                        float y[VN];
+                        IO::unpack(lds128(bu + v * 16), y);
+#pragma unroll
+                        for (int j = 0; j < VN; ++j) {
+                            const float eu = ex2(fmaf(y[j], kLog2e, -muL));
+                            su += eu;
+                            w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
+                        }
                     }
                 }
-            }
             }
             float s = s0 + s1;
             if (tid == NT - 1) {
@@ -677,8 +751,8 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     cf.luL = 0.f;
                     cf.a = a;
                     cf.b = 0.f;
+                    cf.cq = INFINITY;
                     cf.gt = (s * p.w_ce + g_cr) * tg + s * zc * pt;
-                    cf.pad = 0;
                     *coef = cf;
                 }
             } else if (act) {
@@ -734,11 +808,13 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2f(fabsf(a)));
                     cf.neg = a < 0.f;
                     cf.lseL = lseL;
-                    cf.luL = (lse + dlu) * kLog2e;
+                    const float lu = lse + dlu;
+                    const float luL = lu * kLog2e;
+                    cf.luL = luL;
                     cf.a = a;
                     cf.b = s * p.w_kl;
+                    cf.cq = (cf.b > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2f(cf.b)) : INFINITY;
                     cf.gt = s * p.w_ce * tg + s * (zc + p.w_kl) * pt;
-                    cf.pad = 0;
                     *coef = cf;
                     if (rank == 0) {
                         p.ws.row_nll[r] = nll;
@@ -774,7 +850,38 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 continue;
             }
             const RowCoef cf = *coef;
-            if (KL) {
+            if (KL && cf.a > 0.f && cf.b > 0.f) {
+                // g_j = 2^(z_j log2e - cz) - 2^(u_j log2e - cq): both coefficients in the exponents
+                const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
+                const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
+                const uint64_t neg1 = f2_pack(-1.f, -1.f);
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    const uint4 q = lds128(bz + v * 16);
+                    const uint4 qu = lds128(bu + v * 16);
+                    float gv[VN];
+#pragma unroll
+                    for (int k = 0; k < VN / 2; ++k) {
+                        float a0, a1, b0, b1;
+                        f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
+                        f2_unpack(f2_fma(IO::pair(qu, k), L2, ncq), b0, b1);
+                        const uint64_t bq = f2_pack(ex2(b0), ex2(b1));
+                        const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
+                        float g0, g1;
+                        f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
+                        if (v == vt) {
+                            float q0, q1;
+                            f2_unpack(bq, q0, q1);
+                            if (2 * k == kt) g0 = cf.gt - q0;
+                            if (2 * k + 1 == kt) g1 = cf.gt - q1;
+                        }
+                        gv[2 * k] = g0;
+                        gv[2 * k + 1] = g1;
+                    }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                }
+            } else if (KL) {
 #pragma unroll 2
                 for (int v = tid; v < nvec; v += NT) {
                     float x[VN], y[VN], gv[VN], qv[VN];
@@ -1004,6 +1111,23 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
             p.count_out[0] = n;
             p.count_out[1] = p.seg_ids ? *p.ws.n_nonempty : 0;
         }
+    }
+}
+
+// ======================================================================
+// Self-test of the bounded wait used by every kernel above: one thread waits
+// on an mbarrier that nothing ever arrives at, with the given limit, and
+// records whether the wait gave up.  Nothing is copied, so nothing is left in
+// flight when it returns.
+// ======================================================================
+__global__ void wait_selftest_kernel(long long limit_cycles, int* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        fence_mbar_init();
+        const bool done = mbar_wait_bounded(smem_addr(&bar), 0u, limit_cycles);
+        *status = done ? 0 : kErrTimeout;
     }
 }
 

@@ -374,6 +374,21 @@ lmloss_status lmloss_get_device_error(lmloss_handle h)
     return static_cast<lmloss_status>(code);
 }
 
+lmloss_status lmloss_selftest_bounded_wait(lmloss_handle h, long long limit_cycles)
+{
+    if (!h || limit_cycles < 0) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    // the handle's error word doubles as the result slot (it is read back and cleared here)
+    if (cudaMemset(h->ws.err, 0, sizeof(int)) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32>>>(limit_cycles, h->ws.err);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return LMLOSS_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, h->ws.err, sizeof code, cudaMemcpyDeviceToHost) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    if (cudaMemset(h->ws.err, 0, sizeof code) != cudaSuccess) return LMLOSS_ERR_CUDA;
+    return static_cast<lmloss_status>(code);
+}
+
 lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cudaStream_t stream)
 {
     if (!h) return LMLOSS_ERR_INVALID_ARG;

@@ -263,3 +263,40 @@ int orc_grad(int dtype, int64_t n, int64_t V, int64_t ld,
     }
     return failed ? -1 : 0;
 }
+
+/*
+ * Entropy of the softmax of each active row, H = -sum_j p_j log p_j with
+ * p = softmax(z), written to ent[r] (0 on inactive rows).  A side output a
+ * caller may want next to the loss (torchtitan PR 5661, review "Details":
+ * callers reuse the logits, e.g. for entropy).
+ */
+int orc_entropy(int dtype, int64_t n, int64_t V, int64_t ld, const void* logits,
+                const uint8_t* active, double* ent, int nthreads)
+{
+    int failed = 0;
+#pragma omp parallel num_threads(orc_threads(nthreads))
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        if (!z) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n; ++r) {
+            if (!z) continue;
+            if (!active[r]) { ent[r] = 0.0; continue; }
+            orc_load_row(dtype, logits, r, V, ld, z);
+            double lse = orc_logsumexp_skip(z, V, -1);
+            double h = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                double logp = z[j] - lse;
+                double p = exp(logp);
+                if (p == 0.0) continue;          /* 0 log 0 = 0 */
+                h -= p * logp;
+            }
+            ent[r] = h;
+        }
+        free(z);
+    }
+    return failed ? -1 : 0;
+}

@@ -31,6 +31,11 @@ Readings where the pages are silent (each listed in the design notes):
     is divided by the caller's denominator like every other term.
   * A GSPO segment's gradient flows iff s_i*A_i <= clamp(s_i)*A_i (ties flow).
   * Tokens with a negative segment id belong to no segment.
+  * GRPO (named on the Fast-LLM page as a combinable loss that shares the
+    softmax, without a formula) is read as the token-level version of the same
+    clipped surrogate: rho_r = exp(logp_r - old_logp_r),
+    L_r = -min(rho_r A_r, clamp(rho_r, 1-eps_lo, 1+eps_hi) A_r), its gradient
+    flowing iff rho_r A_r <= clamp(rho_r) A_r, reduced like the token terms.
 """
 from __future__ import annotations
 
@@ -81,6 +86,8 @@ def _load():
         lib.orc_forward.restype = ctypes.c_int
         lib.orc_grad.argtypes = [ctypes.c_int, i64, i64, i64, p, p, d, p, p, d, d, d, d, p, p, p, ctypes.c_int]
         lib.orc_grad.restype = ctypes.c_int
+        lib.orc_entropy.argtypes = [ctypes.c_int, i64, i64, i64, p, p, p, ctypes.c_int]
+        lib.orc_entropy.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -109,6 +116,7 @@ class Problem:
     num_segments: int = 0
     advantages: Optional[np.ndarray] = None   # float32 [S]
     old_logprobs: Optional[np.ndarray] = None  # float32 [T]
+    token_advantages: Optional[np.ndarray] = None  # float32 [T]: GRPO (per-token) advantages
     clip_eps_low: float = 0.0
     clip_eps_high: float = 0.0
     reduction: int = REDUCE_TOKEN_MEAN
@@ -154,6 +162,19 @@ def row_forward(P: Problem, active: np.ndarray, nthreads: int = 0):
     if rc != 0:
         raise MemoryError("oracle: out of host memory")
     return tuple(out)
+
+
+def entropy(P: Problem, active: Optional[np.ndarray] = None, nthreads: int = 0) -> np.ndarray:
+    """Per-row entropy of softmax(z) (fp64 [T]); 0 on inactive rows."""
+    lib = _load()
+    act = active_mask(P.targets, P.loss_mask) if active is None else active
+    logits = np.ascontiguousarray(P.logits)
+    out = np.zeros(P.T, dtype=np.float64)
+    rc = lib.orc_entropy(P.dtype, P.T, P.V, P.ld, _ptr(logits), _ptr(np.ascontiguousarray(act, dtype=np.uint8)),
+                         _ptr(out), int(nthreads))
+    if rc != 0:
+        raise MemoryError("oracle: out of host memory")
+    return out
 
 
 @dataclass
@@ -216,7 +237,7 @@ class Result:
     ce: float        # s_tok * sum nll
     z: float         # s_tok * sum alpha * lse^2
     kl_loss: float   # s_tok * sum kl
-    gspo: float      # s_seg * sum L_i
+    gspo: float      # policy term: s_seg * sum L_i (GSPO) or s_tok * sum L_r (GRPO)
     total: float     # ce_weight*ce + z + kl_weight*kl + gspo
     seam: Optional[Seam] = None
     coef: Optional[np.ndarray] = None   # per-row GSPO coefficient c_r
@@ -256,6 +277,23 @@ def forward(P: Problem, nthreads: int = 0) -> Result:
             if act[r] and g >= 0 and seam.flag[g]:
                 A = float(P.advantages[g])
                 coef[r] = s_seg * A * seam.ratio[g] / seam.n[g]
+    if P.token_advantages is not None:
+        if P.segment_ids is not None:
+            raise ValueError("GRPO and GSPO are exclusive")
+        lo, hi = 1.0 - float(P.clip_eps_low), 1.0 + float(P.clip_eps_high)
+        coef = np.zeros(P.T)
+        pol = np.zeros(P.T)
+        for r in range(P.T):
+            if not act[r]:
+                continue
+            A = float(P.token_advantages[r])
+            rho = math.exp(float(logp[r]) - float(P.old_logprobs[r]))
+            c = min(max(rho, lo), hi)
+            pol[r] = -min(rho * A, c * A)
+            if rho * A <= c * A:
+                coef[r] = s_tok * A * rho      # d L_r / d z = A rho (p - onehot)
+        gspo = s_tok * float(np.sum(pol))
+        s_seg = s_tok
     total = P.ce_weight * ce + z + P.kl_weight * kl_loss + gspo
     return Result(act, n_active, s_tok, s_seg, nll, lse, lse_nt, kl, logp,
                   ce, z, kl_loss, gspo, total, seam, coef)

@@ -282,3 +282,27 @@ def test_bad_segment_sets_device_error(dev, handle):
                             ce_weight=0.0, grad="new")
     torch.cuda.synchronize()
     assert handle.device_error() == LMLOSS_ERR_BAD_SEGMENT
+
+
+def test_bounded_wait_gives_up_and_device_stays_usable(dev, handle):
+    """A wait on a barrier nothing arrives at ends with LMLOSS_ERR_TIMEOUT after
+    its limit; the context stays usable (a normal call right after works)."""
+    from lm_head_vocab_gb300 import _lib
+    assert _lib.lmloss_selftest_bounded_wait(handle.handle, 200_000) == _lib.LMLOSS_ERR_TIMEOUT
+    case = _case(dev, "ce_z_bf16", dict(T=16, V=1000))
+    R, g_ref = oracle.forward_backward(case.P)
+    _, out = run(handle, case)
+    compare_all(case, out, R, g_ref, "after the wait self-test")
+
+
+def test_forward_only_with_teacher(dev, handle):
+    """Statistics mode with a teacher and masked rows (no gradient requested)."""
+    case = _case(dev, "ce_z_kl_bf16", dict(T=300, V=20000))
+    R = oracle.forward(case.P)
+    inp = case.device_inputs()
+    out = handle.forward_backward(inp["logits"], inp["targets"], inp["loss_mask"],
+                                  teacher_logits=inp["teacher_logits"], grad=None,
+                                  want=("logp", "lse", "kl", "count"), **case.kwargs())
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    compare_all(case, out, R, None, "forward only with teacher")

@@ -206,7 +206,7 @@ def test_shard_sum_equals_token_mean():
 # Brute force at 50 digits, gradient by central differences of the total loss.
 # --------------------------------------------------------------------------
 def mp_total(z, u, t, act, alpha, w_ce, w_kl, tau, seg, S, adv, old, eps_lo, eps_hi,
-             reduction, denom):
+             reduction, denom, tadv=None):
     T = len(z)
     V = len(z[0])
     N = sum(1 for r in range(T) if act[r])
@@ -227,6 +227,13 @@ def mp_total(z, u, t, act, alpha, w_ce, w_kl, tau, seg, S, adv, old, eps_lo, eps
                 lq = u[r][j] / tau - la
                 kl += mpmath.exp(lq) * (lq - (z[r][j] / tau - lb))
     tot = s_tok * (w_ce * ce + zl + w_kl * kl)
+    if tadv is not None:
+        for r in range(T):
+            if not act[r]:
+                continue
+            rho = mpmath.exp(logp[r] - old[r])
+            c = min(max(rho, 1 - eps_lo), 1 + eps_hi)
+            tot += s_tok * (-min(rho * tadv[r], c * tadv[r]))
     if seg is not None:
         n = [0] * S
         D = [mpmath.mpf(0)] * S
@@ -254,6 +261,8 @@ BRUTE_CASES = [
     ("masked_sum", 3, 4, dict(mask=[1, 0, 1], reduction=0, denominator=5.0, z_alpha=0.02)),
     ("gspo", 3, 3, dict(gspo=True, ce_weight=0.0, z_alpha=0.01)),
     ("gspo_ce_sum", 3, 4, dict(gspo=True, ce_weight=1.0, reduction=0, denominator=3.0)),
+    ("grpo", 4, 3, dict(grpo=True, ce_weight=0.0, z_alpha=0.01)),
+    ("grpo_ce_masked", 4, 4, dict(grpo=True, ce_weight=1.0, mask=[1, 1, 0, 1])),
 ]
 
 
@@ -289,6 +298,17 @@ def test_brute_force_mpmath(name, T, V, kw):
                 old[r] = np.float32(R0.logp[r] - 1.0)
         P.segment_ids, P.num_segments, P.advantages, P.old_logprobs = seg, S, adv, old
         P.clip_eps_low, P.clip_eps_high = eps_lo, eps_hi
+    tadv = None
+    if kw.get("grpo"):
+        # four tokens: two inside the band (one per sign of A), one clipped high
+        # with A > 0 (no gradient), one above the band with A < 0 (flows)
+        R0 = oracle.forward(P, nthreads=1)
+        shifts = [0.05, -0.05, 1.0, 1.0][:T]
+        tadv = np.array([0.7, -1.1, 1.3, -0.4][:T], dtype=np.float32)
+        old = np.array([np.float32(R0.logp[r] - shifts[r]) for r in range(T)], dtype=np.float32)
+        eps_lo, eps_hi = 0.2, 0.2
+        P.token_advantages, P.old_logprobs = tadv, old
+        P.clip_eps_low, P.clip_eps_high = eps_lo, eps_hi
     R, g = run(P)
 
     zm = [[mpmath.mpf(float(x)) for x in row] for row in z]
@@ -300,7 +320,8 @@ def test_brute_force_mpmath(name, T, V, kw):
                 adv=None if adv is None else [mpmath.mpf(float(a)) for a in adv],
                 old=None if old is None else [mpmath.mpf(float(o)) for o in old],
                 eps_lo=mpmath.mpf(eps_lo), eps_hi=mpmath.mpf(eps_hi),
-                reduction=P.reduction, denom=P.denominator)
+                reduction=P.reduction, denom=P.denominator,
+                tadv=None if tadv is None else [mpmath.mpf(float(a)) for a in tadv])
     tot = mp_total(zm, um, **args)
     assert R.total == pytest.approx(float(tot), rel=1e-13, abs=1e-15)
     h = mpmath.mpf("1e-20")
@@ -453,3 +474,32 @@ def test_single_class_row():
     np.testing.assert_allclose(R.lse, [4.0, -2.0])
     # only the z-loss gradient survives: 2 a lse * p / N with p = 1
     np.testing.assert_allclose(g[:, 0], [2 * 0.5 * 4.0 / 2, 2 * 0.5 * -2.0 / 2])
+
+
+# --------------------------------------------------------------------------
+# Entropy side output: closed forms and a 50-digit evaluation.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("V", [1, 2, 9, 4096])
+def test_entropy_uniform_is_log_v(V):
+    z = np.full((3, V), 1.25, dtype=np.float32)
+    H = oracle.entropy(Problem(logits=z, V=V, targets=np.zeros(3, dtype=np.int64)))
+    np.testing.assert_allclose(H, math.log(V), rtol=1e-12, atol=1e-15)
+
+
+def test_entropy_two_class_and_brute():
+    mp.dps = 50
+    rng = np.random.default_rng(11)
+    z = rng.normal(0, 3, size=(5, 2)).astype(np.float32)
+    H = oracle.entropy(Problem(logits=z, V=2, targets=np.zeros(5, dtype=np.int64)))
+    for r in range(5):
+        q = 1 / (1 + mpmath.exp(-(mpmath.mpf(float(z[r, 1])) - mpmath.mpf(float(z[r, 0])))))
+        hb = -(q * mpmath.log(q) + (1 - q) * mpmath.log(1 - q))
+        assert H[r] == pytest.approx(float(hb), rel=1e-12)
+    z = rng.normal(0, 2, size=(3, 7)).astype(np.float32)
+    H = oracle.entropy(Problem(logits=z, V=7, targets=np.array([0, -100, 3])))
+    for r in (0, 2):
+        zs = [mpmath.mpf(float(v)) for v in z[r]]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(v) for v in zs))
+        h = -mpmath.fsum(mpmath.exp(v - lse) * (v - lse) for v in zs)
+        assert H[r] == pytest.approx(float(h), rel=1e-12)
+    assert H[1] == 0.0

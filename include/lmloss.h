@@ -102,7 +102,8 @@ typedef struct {
     double denominator;          /* SUM reduction: every term is divided by this (> 0)     */
 
     void* grad_out;              /* [T, ld] dtype; == logits writes in place; NULL = none  */
-    float* loss_out;             /* [5] total, ce, z, kl, gspo (each after its scale)      */
+    float* loss_out;             /* [5] total, ce, z, kl, policy (GSPO or GRPO), each      */
+                                 /*     after its scale                                    */
     float* logp_out;             /* optional [T]: log p_target = -NLL (0 on inactive rows) */
     float* lse_out;              /* optional [T]: logsumexp of the row (0 on inactive)     */
     float* kl_out;               /* optional [T]: per-row KL (0 on inactive / no teacher)  */
@@ -111,6 +112,12 @@ typedef struct {
     float* seg_ratio_out;        /* optional [num_segments]: s_i = exp(mean log-ratio)     */
     uint8_t* seg_flag_out;       /* optional [num_segments]: 1 iff gradient flows via s_i  */
     float* seg_loss_out;         /* optional [num_segments]: L_i before the GSPO scale     */
+
+    const float* token_advantages; /* [T] GRPO per-token advantages, or NULL: token-level  */
+                                 /* clipped surrogate -min(rho A, clamp(rho) A) with        */
+                                 /* rho = exp(logp - old_logprobs), clip_eps_low/high,     */
+                                 /* scaled like the CE term; exclusive with segment_ids    */
+    float* entropy_out;          /* optional [T]: entropy of softmax(logits) (0 inactive)  */
 } lmloss_args;
 
 /* What the last call launched (for tuning and for benchmark bookkeeping). */
@@ -199,7 +206,7 @@ lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info)
  *
  * Same arguments, results and asynchrony as lmloss_forward_backward, on the
  * current device, without a handle.  It allocates nothing: its workspace is a
- * fixed array of about 0.9 MB inside this library, which every GPU that loads
+ * fixed array of about 1.2 MB inside this library, which every GPU that loads
  * the library holds until the process exits.  Limits: T <= LMLOSS_NOALLOC_MAX_T
  * rows and, with GSPO, num_segments <= LMLOSS_NOALLOC_MAX_SEGMENTS; a larger
  * call returns LMLOSS_ERR_INVALID_ARG before anything is launched.

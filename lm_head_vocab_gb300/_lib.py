@@ -88,6 +88,8 @@ class lmloss_args(ctypes.Structure):
         ("seg_ratio_out", ctypes.c_void_p),
         ("seg_flag_out", ctypes.c_void_p),
         ("seg_loss_out", ctypes.c_void_p),
+        ("token_advantages", ctypes.c_void_p),
+        ("entropy_out", ctypes.c_void_p),
     ]
 
 

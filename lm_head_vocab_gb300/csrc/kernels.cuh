@@ -169,6 +169,7 @@ struct Workspace {
     float* row_nll;      // [max_T]
     float* row_lse;      // [max_T]
     float* row_kl;       // [max_T]
+    float* row_pol;      // [max_T] per-token GRPO loss
     int64_t* n_active;   // [1]
     int64_t* n_nonempty; // [1]
     double* gspo_sum;    // [1]  sum of L_i (unscaled)
@@ -216,6 +217,8 @@ struct CallParams {
     float* seg_ratio_out;
     uint8_t* seg_flag_out;
     float* seg_loss_out;
+    const float* tok_adv;   // GRPO per-token advantages, or null
+    float* entropy_out;
     Workspace ws;
     // fused-kernel launch shape and mode
     int mode;               // kModeFused, kModeStats or kModeGrad
@@ -340,17 +343,19 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 // a later iteration from a global counter and passes it to its peers in its
 // record, so clusters that share SMs with others do not set the pace.
 // ======================================================================
-constexpr int kHdrBytes = 2048;   // mbarriers, row queue, cluster records, warp scratch
+constexpr int kHdrBytes = 3072;   // mbarriers, row queue, cluster records, warp scratch
 constexpr int kMaxCluster = 16;
 
-struct ClusterRec {     // one CTA's partial for the current row (32 bytes)
+struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
     float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
     float zt;           // target logit (on the CTA that owns the target column)
     int next_row;       // rank 0: row for iteration i + nbuf
     int next_t;         // rank 0: its target, or -100 when the row is inactive
+    float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
+    float pad0, pad1, pad2;
 };
-static_assert(sizeof(ClusterRec) == 32, "record is two 16-byte pushes");
+static_assert(sizeof(ClusterRec) == 48, "record is three 16-byte pushes");
 
 struct RowCoef {        // the row's gradient coefficients, shared by the CTA's threads
     float cz;           // a p_j = sign(a) 2^(z_j log2e - cz)
@@ -361,8 +366,139 @@ struct RowCoef {        // the row's gradient coefficients, shared by the CTA's 
     int neg;            // sign of a
 };
 
+template <class IO, int NT>
+__device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int vt, int kt, float mL);
+
+// Pass B sums over the staged interior, target column excluded, with
+// e = 2^a and a = z log2e - mL (mL the slice maximum in base 2):
+//   s = sum e,   b = sum e a  (only with ENT: the entropy partial).
+// A logit of -inf gives e = 0 and e a = NaN in the packed loop; a thread that
+// met one redoes its columns with the guard, which costs nothing otherwise.
+template <class IO, int NT, bool ENT>
+__device__ __forceinline__ void sums_plain(uint32_t bz, int nvec, int tid, int vt, int kt, float mL,
+                                           float& s_out, float& b_out)
+{
+    constexpr int VN = IO::N;
+    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t nm2 = f2_pack(-mL, -mL);
+    uint64_t acc = f2_pack(0.f, 0.f), accb = acc;
+    float s0 = 0.f, b0 = 0.f;
+#pragma unroll 2
+    for (int v = tid; v < nvec; v += NT) {
+        const uint4 q = lds128(bz + v * 16);
+        if (v != vt) {
+            // packed pairs: one f32x2 FMA forms two exponent arguments, one
+            // f32x2 add accumulates two terms
+#pragma unroll
+            for (int k = 0; k < VN / 2; ++k) {
+                const uint64_t arg = f2_fma(IO::pair(q, k), L2, nm2);
+                float a0, a1;
+                f2_unpack(arg, a0, a1);
+                const uint64_t e = f2_pack(ex2(a0), ex2(a1));
+                acc = f2_add(acc, e);
+                if (ENT) accb = f2_fma(e, arg, accb);
+            }
+        } else {
+            float x[VN];
+            IO::unpack(q, x);
+#pragma unroll
+            for (int j = 0; j < VN; ++j)
+                if (j != kt) {
+                    const float a = fmaf(x[j], kLog2e, -mL);
+                    const float e = ex2(a);
+                    s0 += e;
+                    if (ENT && e > 0.f) b0 = fmaf(e, a, b0);
+                }
+        }
+    }
+    float h0, h1;
+    f2_unpack(acc, h0, h1);
+    s_out = s0 + (h0 + h1);
+    if (ENT) {
+        f2_unpack(accb, h0, h1);
+        b0 += h0 + h1;
+        if (isnan(b0) && !isnan(s_out)) b0 = sum_ea_guarded<IO, NT>(bz, nvec, tid, vt, kt, mL);
+    }
+    b_out = b0;
+}
+
+// The same with the teacher slice (guard-free form: no teacher logit is -inf):
+//   su = sum 2^c, c = u log2e - muL,   w = sum 2^c (u - z).
+template <class IO, int NT, bool ENT>
+__device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float mL,
+                                        float muL, float& s_out, float& su_out, float& w_out, float& b_out)
+{
+    constexpr int VN = IO::N;
+    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t nm2 = f2_pack(-mL, -mL);
+    const uint64_t nmu2 = f2_pack(-muL, -muL);
+    const uint64_t neg1 = f2_pack(-1.f, -1.f);
+    uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz, accb = accz;
+#pragma unroll 2
+    for (int v = tid; v < nvec; v += NT) {
+        const uint4 q = lds128(bz + v * 16);
+        const uint4 qu = lds128(bu + v * 16);
+#pragma unroll
+        for (int k = 0; k < VN / 2; ++k) {
+            const uint64_t xz = IO::pair(q, k), xu = IO::pair(qu, k);
+            float a0, a1, u0, u1;
+            const uint64_t argz = f2_fma(xz, L2, nm2);
+            f2_unpack(argz, a0, a1);
+            f2_unpack(f2_fma(xu, L2, nmu2), u0, u1);
+            float e0 = ex2(a0), e1 = ex2(a1);
+            if (v == vt) {
+                if (2 * k == kt) e0 = 0.f;
+                if (2 * k + 1 == kt) e1 = 0.f;
+            }
+            const uint64_t ez = f2_pack(e0, e1);
+            accz = f2_add(accz, ez);
+            if (ENT) accb = f2_fma(ez, argz, accb);
+            const uint64_t eu = f2_pack(ex2(u0), ex2(u1));
+            accu = f2_add(accu, eu);
+            accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
+        }
+    }
+    float h0, h1;
+    f2_unpack(accz, h0, h1);
+    s_out = h0 + h1;
+    f2_unpack(accu, h0, h1);
+    su_out = h0 + h1;
+    f2_unpack(accw, h0, h1);
+    w_out = h0 + h1;
+    float b0 = 0.f;
+    if (ENT) {
+        f2_unpack(accb, h0, h1);
+        b0 = h0 + h1;
+        if (isnan(b0) && !isnan(s_out)) b0 = sum_ea_guarded<IO, NT>(bz, nvec, tid, vt, kt, mL);
+    }
+    b_out = b0;
+}
+
+// b = sum e a over this thread's columns of the interior, skipping e = 0.
+template <class IO, int NT>
+__device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int vt, int kt, float mL)
+{
+    constexpr int VN = IO::N;
+    float b = 0.f;
+    for (int v = tid; v < nvec; v += NT) {
+        float x[VN];
+        IO::unpack(lds128(bz + v * 16), x);
+        for (int j = 0; j < VN; ++j) {
+            const float a = fmaf(x[j], kLog2e, -mL);
+            const float e = ex2(a);
+            if ((v != vt || j != kt) && e > 0.f) b = fmaf(e, a, b);
+        }
+    }
+    return b;
+}
+
+// Occupancy: without a teacher, shared memory admits 1024 threads per SM at the
+// default shape; with one, two CTAs share an SM, so registers are capped to fit two.
+template <bool KL, int NT>
+constexpr int fused_min_blocks() { return NT >= 1024 ? 1 : (KL ? 2 : 1024 / NT); }
+
 template <bool BF16, bool KL, int NT>
-__global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel(const CallParams p)
+__global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel(const CallParams p)
 {
     using IO = Vec<BF16>;
     constexpr int VN = IO::N;
@@ -377,8 +513,8 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
     int* tq = reinterpret_cast<int*>(smem + 48);                         // [4] its target (-100: inactive)
     float* slot = reinterpret_cast<float*>(smem + 64);                   // [1] target logit
     RowCoef* coef = reinterpret_cast<RowCoef*>(smem + 96);               // [1]
-    float* wred = reinterpret_cast<float*>(smem + 256);                  // [6][32]
-    ClusterRec* rec = reinterpret_cast<ClusterRec*>(smem + 1024);        // [2][kMaxCluster]
+    float* wred = reinterpret_cast<float*>(smem + 256);                  // [7][32]
+    ClusterRec* rec = reinterpret_cast<ClusterRec*>(smem + 1280);        // [2][kMaxCluster]
     unsigned char* bufs = smem + kHdrBytes;
 
     const int tid = threadIdx.x;
@@ -467,7 +603,11 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 
         // GSPO gradient pass: the row's statistics and segment coefficient come
         // from the workspace; start those loads now, they are needed after the wait
-        float g_lse = 0.f, g_nll = 0.f, g_cr = 0.f;
+        float g_lse = 0.f, g_nll = 0.f, g_cr = 0.f, g_adv = 0.f, g_old = 0.f;
+        if (p.tok_adv && mode != kModeGrad && warp == 0 && lane == 0 && act && !bad) {
+            g_adv = p.tok_adv[r];
+            g_old = p.old_logp[r];
+        }
         if (mode == kModeGrad && warp == 0 && lane == 0 && act && !bad) {
             g_lse = p.ws.row_lse[r];
             g_nll = p.ws.row_nll[r];
@@ -547,34 +687,10 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             }
             const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
             const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
-            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f;
+            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f;
             if (!KL) {
-                // packed pairs: one f32x2 FMA forms two exponent arguments, one
-                // f32x2 add accumulates two terms
-                const uint64_t L2 = f2_pack(kLog2e, kLog2e);
-                const uint64_t nm2 = f2_pack(-mL, -mL);
-                uint64_t acc = f2_pack(0.f, 0.f);
-#pragma unroll 2
-                for (int v = tid; v < nvec; v += NT) {
-                    const uint4 q = lds128(bz + v * 16);
-                    if (v != vt) {
-#pragma unroll
-                        for (int k = 0; k < VN / 2; ++k) {
-                            float a0, a1;
-                            f2_unpack(f2_fma(IO::pair(q, k), L2, nm2), a0, a1);
-                            acc = f2_add(acc, f2_pack(ex2(a0), ex2(a1)));
-                        }
-                    } else {
-                        float x[VN];
-                        IO::unpack(q, x);
-#pragma unroll
-                        for (int j = 0; j < VN; ++j)
-                            if (j != kt) s0 += ex2(fmaf(x[j], kLog2e, -mL));
-                    }
-                }
-                float h0, h1;
-                f2_unpack(acc, h0, h1);
-                s1 = h0 + h1;
+                if (p.entropy_out) sums_plain<IO, NT, true>(bz, nvec, tid, vt, kt, mL, s0, b0);
+                else sums_plain<IO, NT, false>(bz, nvec, tid, vt, kt, mL, s0, b0);
             }
             if (KL) {
                 // with no -inf teacher logit in the slice, e^(u-mu) (u - z) needs no guard
@@ -582,47 +698,20 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) un_cta = fminf(un_cta, __shfl_xor_sync(0xffffffffu, un_cta, off));
                 if (un_cta > -INFINITY) {
-                    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
-                    const uint64_t nm2 = f2_pack(-mL, -mL);
-                    const uint64_t nmu2 = f2_pack(-muL, -muL);
-                    const uint64_t neg1 = f2_pack(-1.f, -1.f);
-                    uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz;
-#pragma unroll 2
-                    for (int v = tid; v < nvec; v += NT) {
-                        const uint4 q = lds128(bz + v * 16);
-                        const uint4 qu = lds128(bu + v * 16);
-#pragma unroll
-                        for (int k = 0; k < VN / 2; ++k) {
-                            const uint64_t xz = IO::pair(q, k), xu = IO::pair(qu, k);
-                            float a0, a1, b0, b1;
-                            f2_unpack(f2_fma(xz, L2, nm2), a0, a1);
-                            f2_unpack(f2_fma(xu, L2, nmu2), b0, b1);
-                            float e0 = ex2(a0), e1 = ex2(a1);
-                            if (v == vt) {
-                                if (2 * k == kt) e0 = 0.f;
-                                if (2 * k + 1 == kt) e1 = 0.f;
-                            }
-                            accz = f2_add(accz, f2_pack(e0, e1));
-                            const uint64_t eu = f2_pack(ex2(b0), ex2(b1));
-                            accu = f2_add(accu, eu);
-                            accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
-                        }
-                    }
-                    float h0, h1;
-                    f2_unpack(accz, h0, h1);
-                    s0 = h0 + h1;
-                    f2_unpack(accu, h0, h1);
-                    su = h0 + h1;
-                    f2_unpack(accw, h0, h1);
-                    w = h0 + h1;
+                    if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
+                    else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
                 } else {
 #pragma unroll 2
                     for (int v = tid; v < nvec; v += NT) {
                         float x[VN];
                         IO::unpack(lds128(bz + v * 16), x);
                         float e[VN];
+                        float ar[VN];
 #pragma unroll
-                        for (int j = 0; j < VN; ++j) e[j] = ex2(fmaf(x[j], kLog2e, -mL));
+                        for (int j = 0; j < VN; ++j) {
+                            ar[j] = fmaf(x[j], kLog2e, -mL);
+                            e[j] = ex2(ar[j]);
+                        }
                         if (v == vt) {
 #pragma unroll
                             for (int j = 0; j < VN; ++j)
@@ -630,6 +719,9 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                         }
 #pragma unroll
                         for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
+#pragma unroll
+                        for (int j = 0; j < VN; ++j)
+                            if (e[j] > 0.f) b0 = fmaf(e[j], ar[j], b0);
                         float y[VN];
                         IO::unpack(lds128(bu + v * 16), y);
 #pragma unroll
@@ -647,7 +739,12 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
-                        if (j != t) s += ex2(fmaf(x, kLog2e, -mL));
+                        if (j != t) {
+                            const float a = fmaf(x, kLog2e, -mL);
+                            const float e = ex2(a);
+                            s += e;
+                            if (e > 0.f) b0 = fmaf(e, a, b0);
+                        }
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             const float eu = ex2(fmaf(y, kLog2e, -muL));
@@ -660,6 +757,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 s += __shfl_xor_sync(0xffffffffu, s, off);
+                b0 += __shfl_xor_sync(0xffffffffu, b0, off);
                 if (KL) {
                     su += __shfl_xor_sync(0xffffffffu, su, off);
                     w += __shfl_xor_sync(0xffffffffu, w, off);
@@ -667,6 +765,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             }
             if (lane == 0) {
                 wred[64 + warp] = s;
+                wred[192 + warp] = b0;
                 if (KL) { wred[96 + warp] = su; wred[128 + warp] = w; }
             }
         }
@@ -674,9 +773,10 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 
         // ---- publish this CTA's record
         if (warp == 0) {
-            float s = 0.f, su = 0.f, w = 0.f;
+            float s = 0.f, su = 0.f, w = 0.f, bc = 0.f;
             if (act) {
                 s = (lane < NW) ? wred[64 + lane] : 0.f;
+                bc = (lane < NW) ? wred[192 + lane] : 0.f;
                 if (KL) {
                     su = (lane < NW) ? wred[96 + lane] : 0.f;
                     w = (lane < NW) ? wred[128 + lane] : 0.f;
@@ -684,6 +784,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     s += __shfl_xor_sync(0xffffffffu, s, off);
+                    bc += __shfl_xor_sync(0xffffffffu, bc, off);
                     if (KL) {
                         su += __shfl_xor_sync(0xffffffffu, su, off);
                         w += __shfl_xor_sync(0xffffffffu, w, off);
@@ -696,7 +797,13 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
                 const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
                 R.m = m_cta;
-                R.s = (m_cta == -INFINITY) ? s : s * ex2(-fmaf(m_cta, kLog2e, -mL));
+                // e = 2^(z log2e - mL) = e^(z - m) 2^delta and bc sums e (z log2e - mL), so
+                // sum e^(z - m) (z - m) = 2^-delta (bc - delta s) / log2e
+                const float delta = (m_cta == -INFINITY) ? 0.f : fmaf(m_cta, kLog2e, -mL);
+                const float f = ex2(-delta);
+                R.s = s * f;
+                R.bc = (bc - delta * s) * f * (1.0f / kLog2e);
+                R.pad0 = R.pad1 = R.pad2 = 0.f;
                 R.mu = mu_cta;
                 const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, kLog2e, -muL));
                 R.su = su * fu;
@@ -715,6 +822,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     const uint32_t bar = dsmem_map(my_bar, static_cast<uint32_t>(c));
                     st_async_v4(dst, Rv[0], bar);
                     st_async_v4(dst + 16, Rv[1], bar);
+                    st_async_v4(dst + 32, Rv[2], bar);
                 }
             }
         }
@@ -728,7 +836,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
             }
             ClusterRec q;
             q.m = -INFINITY; q.s = 0.f; q.mu = -INFINITY; q.su = 0.f; q.w = 0.f; q.zt = 0.f;
-            q.next_row = 0; q.next_t = -100;
+            q.next_row = 0; q.next_t = -100; q.bc = 0.f;
             if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
@@ -759,7 +867,10 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                 float M = q.m;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-                float S = q.s * rescale(q.m, M);
+                const float fz = rescale(q.m, M);
+                float S = q.s * fz;
+                // sum e^(z - M) (z - M) over this CTA's non-target columns
+                float Bc = (q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
                 float Mu = q.mu, Su = 0.f, W = 0.f;
                 if (KL) {
 #pragma unroll
@@ -771,6 +882,7 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     S += __shfl_xor_sync(0xffffffffu, S, off);
+                    Bc += __shfl_xor_sync(0xffffffffu, Bc, off);
                     if (KL) {
                         Su += __shfl_xor_sync(0xffffffffu, Su, off);
                         W += __shfl_xor_sync(0xffffffffu, W, off);
@@ -800,7 +912,17 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     }
                     const float s = s_tok;
                     const float zc = 2.f * p.alpha * lse;
-                    const float a = s * (p.w_ce + zc + p.w_kl);
+                    // GRPO, token level: rho = exp(logp - old), L = -min(rho A, clamp(rho) A);
+                    // when the unclipped branch is taken its gradient is s A rho (p - onehot)
+                    float c_r = 0.f, pol = 0.f;
+                    if (p.tok_adv) {
+                        const float rho = expf(-nll - g_old);
+                        const float rc = fminf(fmaxf(rho, 1.f - p.eps_lo), 1.f + p.eps_hi);
+                        pol = -fminf(rho * g_adv, rc * g_adv);
+                        if (rho * g_adv <= rc * g_adv) c_r = s * g_adv * rho;
+                        if (isnan(rho) || isnan(g_adv)) { pol = rho + g_adv; c_r = pol; }
+                    }
+                    const float a = s * (p.w_ce + zc + p.w_kl) + c_r;
                     RowCoef cf;
                     // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
                     const float lseL = lse * kLog2e;
@@ -814,19 +936,31 @@ __global__ void __launch_bounds__(NT, (NT >= 1024 ? 1 : 1024 / NT)) fused_kernel
                     cf.a = a;
                     cf.b = s * p.w_kl;
                     cf.cq = (cf.b > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2f(cf.b)) : INFINITY;
-                    cf.gt = s * p.w_ce * tg + s * (zc + p.w_kl) * pt;
+                    cf.gt = (s * p.w_ce + c_r) * tg + s * (zc + p.w_kl) * pt;
                     *coef = cf;
                     if (rank == 0) {
                         p.ws.row_nll[r] = nll;
                         p.ws.row_lse[r] = lse;
                         p.ws.row_kl[r] = kl;
+                        p.ws.row_pol[r] = pol;
+                        if (p.entropy_out) {
+                            // H = lse - E_p[z] = (lse - M) - p_nt E_nt[z - M] - p_t (z_t - M)
+                            const float pnt = -expm1f(-nll);
+                            float h = lse - zt;     // only the target column carries mass
+                            if (S > 0.f) {
+                                h = (lnS + sp_neg) - pnt * (Bc / S);
+                                if (pt > 0.f) h -= pt * (zt - M);
+                            }
+                            p.entropy_out[r] = h;
+                        }
                         if (p.logp_out) p.logp_out[r] = -nll;
                         if (p.lse_out) p.lse_out[r] = lse;
                         if (p.kl_out) p.kl_out[r] = kl;
                     }
                 }
             } else if (lane == 0 && rank == 0 && mode != kModeGrad) {
-                p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f;
+                p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f; p.ws.row_pol[r] = 0.f;
+                if (p.entropy_out) p.entropy_out[r] = 0.f;
                 if (p.logp_out) p.logp_out[r] = 0.f;
                 if (p.lse_out) p.lse_out[r] = 0.f;
                 if (p.kl_out) p.kl_out[r] = 0.f;
@@ -1059,48 +1193,54 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
 // ======================================================================
 __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
 {
-    __shared__ double part[3][8];
+    __shared__ double part[4][8];
     __shared__ bool last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5, nb = gridDim.x;
     const int64_t chunk = (p.T + nb - 1) / nb;
     const int64_t r0 = blockIdx.x * chunk, r1 = min(p.T, r0 + chunk);
-    double a = 0.0, b = 0.0, c = 0.0;
+    double a = 0.0, b = 0.0, c = 0.0, d = 0.0;
     for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
         const double lse = p.ws.row_lse[r];
         a += p.ws.row_nll[r];
         b += lse * lse;
         c += p.ws.row_kl[r];
+        if (p.tok_adv) d += p.ws.row_pol[r];
     }
     for (int off = 16; off > 0; off >>= 1) {
         a += __shfl_xor_sync(0xffffffffu, a, off);
         b += __shfl_xor_sync(0xffffffffu, b, off);
         c += __shfl_xor_sync(0xffffffffu, c, off);
+        d += __shfl_xor_sync(0xffffffffu, d, off);
     }
-    if (lane == 0) { part[0][warp] = a; part[1][warp] = b; part[2][warp] = c; }
+    if (lane == 0) { part[0][warp] = a; part[1][warp] = b; part[2][warp] = c; part[3][warp] = d; }
     __syncthreads();
     if (tid == 0) {
-        double sa = 0.0, sb = 0.0, sc = 0.0;
-        for (int k = 0; k < nw; ++k) { sa += part[0][k]; sb += part[1][k]; sc += part[2][k]; }
-        p.ws.red_part[3 * blockIdx.x] = sa;
-        p.ws.red_part[3 * blockIdx.x + 1] = sb;
-        p.ws.red_part[3 * blockIdx.x + 2] = sc;
+        double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
+        for (int k = 0; k < nw; ++k) { sa += part[0][k]; sb += part[1][k]; sc += part[2][k]; sd += part[3][k]; }
+        p.ws.red_part[4 * blockIdx.x] = sa;
+        p.ws.red_part[4 * blockIdx.x + 1] = sb;
+        p.ws.red_part[4 * blockIdx.x + 2] = sc;
+        p.ws.red_part[4 * blockIdx.x + 3] = sd;
         __threadfence();
         last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
     }
     __syncthreads();
     if (last && tid == 0) {
         __threadfence();
-        double sa = 0.0, sb = 0.0, sc = 0.0;
+        double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
         const volatile double* rp = p.ws.red_part;
-        for (int k = 0; k < nb; ++k) { sa += rp[3 * k]; sb += rp[3 * k + 1]; sc += rp[3 * k + 2]; }
+        for (int k = 0; k < nb; ++k) {
+            sa += rp[4 * k]; sb += rp[4 * k + 1]; sc += rp[4 * k + 2]; sd += rp[4 * k + 3];
+        }
         p.ws.done[1] = 0u;
         const int64_t n = *p.ws.n_active;
         const double s = (p.reduction == 1) ? (n > 0 ? 1.0 / static_cast<double>(n) : 0.0) : p.inv_denominator;
         const double ce = s * sa;
         const double z = s * static_cast<double>(p.alpha) * sb;
         const double kl = s * sc;
-        double gspo = 0.0;
+        double gspo = 0.0;                       // the policy term: GSPO or GRPO
         if (p.seg_ids) gspo = *p.ws.s_seg * *p.ws.gspo_sum;
+        else if (p.tok_adv) gspo = s * sd;
         const double total = static_cast<double>(p.w_ce) * ce + z + static_cast<double>(p.w_kl) * kl + gspo;
         p.loss_out[0] = static_cast<float>(total);
         p.loss_out[1] = static_cast<float>(ce);

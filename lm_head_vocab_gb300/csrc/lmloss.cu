@@ -85,6 +85,11 @@ lmloss_status check(const lmloss_args* a)
         if (!(a->clip_eps_low >= 0.f) || !(a->clip_eps_high >= 0.f)) return LMLOSS_ERR_INVALID_ARG;
         if (a->teacher_logits) return LMLOSS_ERR_UNSUPPORTED;
     }
+    if (a->token_advantages) {
+        if (a->segment_ids) return LMLOSS_ERR_INVALID_ARG;   // one policy term per call
+        if (a->T > 0 && !a->old_logprobs) return LMLOSS_ERR_INVALID_ARG;
+        if (!(a->clip_eps_low >= 0.f) || !(a->clip_eps_high >= 0.f)) return LMLOSS_ERR_INVALID_ARG;
+    }
     return LMLOSS_OK;
 }
 
@@ -268,11 +273,11 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     const size_t S = static_cast<size_t>(max_segments > 0 ? max_segments : 1);
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
-    const size_t o_nll = take(4 * T), o_lse = take(4 * T), o_kl = take(4 * T);
+    const size_t o_nll = take(4 * T), o_lse = take(4 * T), o_kl = take(4 * T), o_pol = take(4 * T);
     const size_t o_scal = take(64);
     const size_t o_sn = take(4 * S), o_dq = take(8 * S), o_aq = take(8 * S), o_nf = take(12 * S), o_coef = take(4 * S);
     const size_t o_ctr = take(16);
-    const size_t o_cnt = take(8 * kRedBlocks), o_red = take(24 * kRedBlocks), o_done = take(16);
+    const size_t o_cnt = take(8 * kRedBlocks), o_red = take(32 * kRedBlocks), o_done = take(16);
     const size_t o_err = take(16);
     if (cudaMalloc(&h->ws_mem, off) != cudaSuccess) {
         delete h;
@@ -282,6 +287,7 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     h->ws.row_nll = reinterpret_cast<float*>(base + o_nll);
     h->ws.row_lse = reinterpret_cast<float*>(base + o_lse);
     h->ws.row_kl = reinterpret_cast<float*>(base + o_kl);
+    h->ws.row_pol = reinterpret_cast<float*>(base + o_pol);
     h->ws.n_active = reinterpret_cast<int64_t*>(base + o_scal);
     h->ws.n_nonempty = reinterpret_cast<int64_t*>(base + o_scal + 8);
     h->ws.gspo_sum = reinterpret_cast<double*>(base + o_scal + 16);
@@ -431,6 +437,8 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     p.seg_ratio_out = a->seg_ratio_out;
     p.seg_flag_out = a->seg_flag_out;
     p.seg_loss_out = a->seg_loss_out;
+    p.tok_adv = a->token_advantages;
+    p.entropy_out = a->entropy_out;
     p.ws = h->ws;
 
     lmloss_call_info info{};
@@ -514,7 +522,8 @@ struct NoAllocLayout {
     static constexpr size_t nll = 0;
     static constexpr size_t lse = nll + na_align(4 * kNoAllocMaxT);
     static constexpr size_t kl = lse + na_align(4 * kNoAllocMaxT);
-    static constexpr size_t scal = kl + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t pol = kl + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t scal = pol + na_align(4 * kNoAllocMaxT);
     static constexpr size_t seg_n = scal + na_align(64);
     static constexpr size_t seg_dq = seg_n + na_align(4 * kNoAllocMaxS);
     static constexpr size_t seg_absq = seg_dq + na_align(8 * kNoAllocMaxS);
@@ -523,12 +532,12 @@ struct NoAllocLayout {
     static constexpr size_t counter = seg_coef + na_align(4 * kNoAllocMaxS);
     static constexpr size_t cnt_part = counter + na_align(16);
     static constexpr size_t red_part = cnt_part + na_align(8 * kRedBlocks);
-    static constexpr size_t done = red_part + na_align(24 * kRedBlocks);
+    static constexpr size_t done = red_part + na_align(32 * kRedBlocks);
     static constexpr size_t err = done + na_align(16);
     static constexpr size_t total = err + na_align(16);
 };
 
-// The workspace itself (about 0.9 MB).  It is zero when the library loads, as
+// The workspace itself (about 1.2 MB).  It is zero when the library loads, as
 // the block counters that must start every call at zero require; the kernels
 // return those counters to zero at the end of each call and clear the
 // per-call accumulators themselves at its start.
@@ -595,6 +604,7 @@ extern "C" lmloss_status lmloss_forward_backward_noalloc(const lmloss_args* a, c
     ctx.ws.row_nll = reinterpret_cast<float*>(b + L::nll);
     ctx.ws.row_lse = reinterpret_cast<float*>(b + L::lse);
     ctx.ws.row_kl = reinterpret_cast<float*>(b + L::kl);
+    ctx.ws.row_pol = reinterpret_cast<float*>(b + L::pol);
     ctx.ws.n_active = reinterpret_cast<int64_t*>(b + L::scal);
     ctx.ws.n_nonempty = reinterpret_cast<int64_t*>(b + L::scal + 8);
     ctx.ws.gspo_sum = reinterpret_cast<double*>(b + L::scal + 16);

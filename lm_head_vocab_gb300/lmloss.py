@@ -45,6 +45,7 @@ class Outputs:
     seg_ratio: Optional[torch.Tensor] = None
     seg_flag: Optional[torch.Tensor] = None
     seg_loss: Optional[torch.Tensor] = None
+    entropy: Optional[torch.Tensor] = None
 
 
 class LMLoss:
@@ -96,7 +97,7 @@ class LMLoss:
                    ce_weight: float = 1.0, z_alpha: float = 0.0, teacher_logits=None,
                    kl_weight: float = 0.0, temperature: float = 1.0, segment_ids=None,
                    num_segments: Optional[int] = None, advantages=None, old_logprobs=None,
-                   clip_eps_low: float = 0.0, clip_eps_high: float = 0.0,
+                   clip_eps_low: float = 0.0, clip_eps_high: float = 0.0, token_advantages=None,
                    reduction: str = "token_mean", denominator: float = 1.0,
                    grad: Union[None, str, torch.Tensor] = "new", V: Optional[int] = None,
                    want=("logp", "lse")):
@@ -133,7 +134,12 @@ class LMLoss:
             S = int(num_segments) if num_segments is not None else int(advantages.numel())
             _need(advantages, "advantages", torch.float32, S, dev)
             _need(old_logprobs, "old_logprobs", torch.float32, T, dev)
+        if token_advantages is not None:
+            _need(token_advantages, "token_advantages", torch.float32, T, dev)
+            _need(old_logprobs, "old_logprobs", torch.float32, T, dev)
         f32 = dict(dtype=torch.float32, device=dev)
+        if "entropy" in want:
+            out.entropy = torch.empty(T, **f32)
         if "logp" in want:
             out.logp = torch.empty(T, **f32)
         if "lse" in want:
@@ -177,7 +183,10 @@ class LMLoss:
         a.seg_ratio_out = _ptr(out.seg_ratio)
         a.seg_flag_out = _ptr(out.seg_flag)
         a.seg_loss_out = _ptr(out.seg_loss)
-        keep = (logits, targets, loss_mask, teacher_logits, segment_ids, advantages, old_logprobs)
+        a.token_advantages = _ptr(token_advantages)
+        a.entropy_out = _ptr(out.entropy)
+        keep = (logits, targets, loss_mask, teacher_logits, segment_ids, advantages, old_logprobs,
+                token_advantages)
         return a, out, keep
 
     def call(self, args: "_lib.lmloss_args", stream: Optional[torch.cuda.Stream] = None):

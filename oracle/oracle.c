@@ -286,13 +286,25 @@ int orc_entropy(int dtype, int64_t n, int64_t V, int64_t ld, const void* logits,
             if (!z) continue;
             if (!active[r]) { ent[r] = 0.0; continue; }
             orc_load_row(dtype, logits, r, V, ld, z);
-            double lse = orc_logsumexp_skip(z, V, -1);
+            /* -log p_j = lse - z_j.  For the largest entry k that difference is
+             * log(1 + t), t = sum_{j != k} exp(z_j - z_k), which fp64 would round
+             * to 0 as lse - z_k once p_k is within 1e-16 of 1; take it through
+             * log1p, and lse - z_j = (z_k - z_j) + log1p(t) for the others. */
+            int64_t k = 0;
+            for (int64_t j = 1; j < V; ++j)
+                if (z[j] > z[k]) k = j;
             double h = 0.0;
-            for (int64_t j = 0; j < V; ++j) {
-                double logp = z[j] - lse;
-                double p = exp(logp);
-                if (p == 0.0) continue;          /* 0 log 0 = 0 */
-                h -= p * logp;
+            if (z[k] > -INFINITY) {
+                double t = 0.0;
+                for (int64_t j = 0; j < V; ++j)
+                    if (j != k) t += exp(z[j] - z[k]);
+                const double l1 = log1p(t);
+                for (int64_t j = 0; j < V; ++j) {
+                    double nlogp = (j == k) ? l1 : (z[k] - z[j]) + l1;
+                    double p = exp(-nlogp);
+                    if (p == 0.0) continue;          /* 0 log 0 = 0 */
+                    h += p * nlogp;
+                }
             }
             ent[r] = h;
         }

@@ -28,6 +28,9 @@ MUTATIONS = [
     ("kl_wrong_log_term", "kl += q * (log_q - (b[j] - lse_b));", "kl += q * (log_q - (b[j] - lse_a));"),
     ("logaddexp_wrong_sign", "return hi + log1p(exp(lo - hi));", "return hi - log1p(exp(lo - hi));"),
     ("gspo_coef_uses_onehot_only", "g[j] = s_tok * term + c_r * p_minus_onehot;", "g[j] = s_tok * term + c_r * p;"),
+    ("entropy_drops_log1p_for_others", "double nlogp = (j == k) ? l1 : (z[k] - z[j]) + l1;",
+     "double nlogp = (j == k) ? l1 : (z[k] - z[j]);"),
+    ("entropy_max_term_rounds_to_zero", "double nlogp = (j == k) ? l1 :", "double nlogp = (j == k) ? 0.0 :"),
     ("wrong_row_stride", "out[j] = orc_elem(dtype, base, r * ld + j);", "out[j] = orc_elem(dtype, base, r * V + j);"),
 ]
 
@@ -46,6 +49,8 @@ def _build_mutant(tmp_path, old, new):
     lib.orc_forward.restype = ctypes.c_int
     lib.orc_grad.argtypes = real.orc_grad.argtypes
     lib.orc_grad.restype = ctypes.c_int
+    lib.orc_entropy.argtypes = real.orc_entropy.argtypes
+    lib.orc_entropy.restype = ctypes.c_int
     return lib
 
 
@@ -61,6 +66,9 @@ def _pins_pass():
         lambda: pins.test_row_sums(),
         lambda: pins.test_torch_fp64_autograd(0),
         lambda: pins.test_gspo_ratio_one(),
+        lambda: pins.test_entropy_uniform_is_log_v(9),
+        lambda: pins.test_entropy_two_class_and_brute(),
+        lambda: pins.test_entropy_confident_rows(60.0),
         lambda: pins.test_brute_force_mpmath("kl_tau2", 2, 3, dict(teacher=True, kl_weight=0.7,
                                                                     temperature=2.0, z_alpha=0.01)),
     ]

@@ -503,3 +503,25 @@ def test_entropy_two_class_and_brute():
         h = -mpmath.fsum(mpmath.exp(v - lse) * (v - lse) for v in zs)
         assert H[r] == pytest.approx(float(h), rel=1e-12)
     assert H[1] == 0.0
+
+
+@pytest.mark.parametrize("margin", [40.0, 60.0, 90.0])
+def test_entropy_confident_rows(margin):
+    """A row whose largest logit leads by a wide margin: p of that entry is
+    within 1e-17 of 1, so -log p must not round to 0 (50-digit reference)."""
+    mp.dps = 60
+    rng = np.random.default_rng(int(margin))
+    z = rng.normal(0, 1, size=(2, 64)).astype(np.float32)
+    z[0, 5] = np.float32(margin)
+    z[1, :] = 0.0
+    z[1, 9] = np.float32(margin)            # two-level row: closed form below
+    H = oracle.entropy(Problem(logits=z, V=64, targets=np.zeros(2, dtype=np.int64)))
+    zs = [mpmath.mpf(float(v)) for v in z[0]]
+    lse = mpmath.log(mpmath.fsum(mpmath.exp(v) for v in zs))
+    h = -mpmath.fsum(mpmath.exp(v - lse) * (v - lse) for v in zs)
+    assert H[0] == pytest.approx(float(h), rel=1e-12)
+    # one entry at m, 63 at 0: q = 63 e^-m / (1 + 63 e^-m) spread evenly over 63
+    m = mpmath.mpf(float(margin))
+    q = 63 * mpmath.exp(-m) / (1 + 63 * mpmath.exp(-m))
+    hb = -((1 - q) * mpmath.log(1 - q) + q * mpmath.log(q / 63))
+    assert H[1] == pytest.approx(float(hb), rel=1e-12)

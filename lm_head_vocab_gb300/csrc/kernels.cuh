@@ -944,13 +944,15 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         p.ws.row_kl[r] = kl;
                         p.ws.row_pol[r] = pol;
                         if (p.entropy_out) {
-                            // H = lse - E_p[z] = (lse - M) - p_nt E_nt[z - M] - p_t (z_t - M)
+                            // H = sum p (-log p): the target gives p_t NLL; a non-target j gives
+                            // p_j (lse - z_j) with p_j = p_nt e^(z_j - M) / S and
+                            // lse - z_j = ln S + softplus(-d) - (z_j - M), so
+                            //   H = p_t NLL + p_nt (ln S - B/S + softplus(-d)),
+                            // every term non-negative (ln S - B/S is the entropy of the
+                            // non-target distribution), hence no cancellation on confident rows
                             const float pnt = -expm1f(-nll);
-                            float h = lse - zt;     // only the target column carries mass
-                            if (S > 0.f) {
-                                h = (lnS + sp_neg) - pnt * (Bc / S);
-                                if (pt > 0.f) h -= pt * (zt - M);
-                            }
+                            float h = (pt > 0.f) ? pt * nll : 0.f;
+                            if (S > 0.f) h = fmaf(pnt, (lnS - Bc / S) + sp_neg, h);
                             p.entropy_out[r] = h;
                         }
                         if (p.logp_out) p.logp_out[r] = -nll;

@@ -527,6 +527,12 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     const int64_t c1 = min(p.V, c0 + p.slice);
     const int nbuf = p.nbuf;
     const float s_tok = token_scale(p);
+    // Kernel-wide constants of the row coefficients: b = s w_kl and, when no
+    // per-row term enters it (no z-loss, no policy term), a = s (w_ce + w_kl).
+    const float b_kl = s_tok * p.w_kl;
+    const float log2_b = (b_kl > 0.f) ? log2f(b_kl) : 0.f;
+    const bool a_fixed = p.alpha == 0.f && !p.tok_adv;
+    const float log2_a_fixed = log2f(fabsf(s_tok * (p.w_ce + p.w_kl)));
     const int mode = p.mode;
 
     auto buf_addr = [&](int b, int a) -> uint32_t {
@@ -600,6 +606,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             set_error(p.ws.err, kErrTimeout);
             failed = true;
         }
+
+        // the claimed row's target: loaded now, while the passes run, because the
+        // whole cluster waits on rank 0's record that carries it
+        int next_t_pf = -100;
+        if (tid == 0 && rank == 0 && claim_row < p.T) next_t_pf = row_target(p, claim_row);
 
         // GSPO gradient pass: the row's statistics and segment coefficient come
         // from the workspace; start those loads now, they are needed after the wait
@@ -791,39 +802,40 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     }
                 }
             }
-            if (lane == 0) {
-                ClusterRec R;
-                // the sums were taken against round(m log2e); undo that rounding exactly
-                const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
-                const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
-                R.m = m_cta;
-                // e = 2^(z log2e - mL) = e^(z - m) 2^delta and bc sums e (z log2e - mL), so
-                // sum e^(z - m) (z - m) = 2^-delta (bc - delta s) / log2e
-                const float delta = (m_cta == -INFINITY) ? 0.f : fmaf(m_cta, kLog2e, -mL);
-                const float f = ex2(-delta);
-                R.s = s * f;
-                R.bc = (bc - delta * s) * f * (1.0f / kLog2e);
-                R.pad0 = R.pad1 = R.pad2 = 0.f;
-                R.mu = mu_cta;
-                const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, kLog2e, -muL));
-                R.su = su * fu;
-                R.w = w * fu;
-                R.zt = owner ? slot[0] : 0.f;
-                R.next_row = (rank == 0) ? claim_row : 0;
-                R.next_t = (rank == 0 && claim_row < p.T) ? row_target(p, claim_row) : -100;
-                // push the record into slot [i & 1][rank] of every CTA of the cluster;
-                // the bytes complete on that CTA's record barrier for this parity
-                const uint4* Rv = reinterpret_cast<const uint4*>(&R);
-                const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
-                const uint32_t my_bar = smem_addr(&rbar[i & 1]);
-                mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C * sizeof(ClusterRec)));
-                for (int c = 0; c < C; ++c) {
-                    const uint32_t dst = dsmem_map(my_slot, static_cast<uint32_t>(c));
-                    const uint32_t bar = dsmem_map(my_bar, static_cast<uint32_t>(c));
-                    st_async_v4(dst, Rv[0], bar);
-                    st_async_v4(dst + 16, Rv[1], bar);
-                    st_async_v4(dst + 32, Rv[2], bar);
-                }
+            // every lane holds the CTA totals and builds the same record; lane c
+            // pushes it into slot [i & 1][rank] of CTA c, whose record barrier for
+            // this parity counts the bytes
+            const int claim_b = __shfl_sync(0xffffffffu, claim_row, 0);
+            const int next_t_b = __shfl_sync(0xffffffffu, next_t_pf, 0);
+            ClusterRec R;
+            // the sums were taken against round(m log2e); undo that rounding exactly
+            const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
+            const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
+            R.m = m_cta;
+            // e = 2^(z log2e - mL) = e^(z - m) 2^delta and bc sums e (z log2e - mL), so
+            // sum e^(z - m) (z - m) = 2^-delta (bc - delta s) / log2e
+            const float delta = (m_cta == -INFINITY) ? 0.f : fmaf(m_cta, kLog2e, -mL);
+            const float f = ex2(-delta);
+            R.s = s * f;
+            R.bc = (bc - delta * s) * f * (1.0f / kLog2e);
+            R.pad0 = R.pad1 = R.pad2 = 0.f;
+            R.mu = mu_cta;
+            const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, kLog2e, -muL));
+            R.su = su * fu;
+            R.w = w * fu;
+            R.zt = owner ? slot[0] : 0.f;   // exactly 0 in every CTA but the target's owner
+            R.next_row = (rank == 0) ? claim_b : 0;
+            R.next_t = (rank == 0) ? next_t_b : -100;
+            const uint4* Rv = reinterpret_cast<const uint4*>(&R);
+            const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
+            const uint32_t my_bar = smem_addr(&rbar[i & 1]);
+            if (lane == 0) mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C * sizeof(ClusterRec)));
+            if (lane < C) {
+                const uint32_t dst = dsmem_map(my_slot, static_cast<uint32_t>(lane));
+                const uint32_t bar = dsmem_map(my_bar, static_cast<uint32_t>(lane));
+                st_async_v4(dst, Rv[0], bar);
+                st_async_v4(dst + 16, Rv[1], bar);
+                st_async_v4(dst + 32, Rv[2], bar);
             }
         }
 
@@ -871,6 +883,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 float S = q.s * fz;
                 // sum e^(z - M) (z - M) over this CTA's non-target columns
                 float Bc = (q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
+                float Zt = q.zt;   // summed below: every record but the owner's holds exactly 0
                 float Mu = q.mu, Su = 0.f, W = 0.f;
                 if (KL) {
 #pragma unroll
@@ -883,13 +896,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 for (int off = 16; off > 0; off >>= 1) {
                     S += __shfl_xor_sync(0xffffffffu, S, off);
                     Bc += __shfl_xor_sync(0xffffffffu, Bc, off);
+                    Zt += __shfl_xor_sync(0xffffffffu, Zt, off);
                     if (KL) {
                         Su += __shfl_xor_sync(0xffffffffu, Su, off);
                         W += __shfl_xor_sync(0xffffffffu, W, off);
                     }
                 }
-                const int own = bad ? 0 : static_cast<int>(t / p.slice);
-                const float ztf = __shfl_sync(0xffffffffu, q.zt, own);
+                const float ztf = Zt;
                 if (lane == 0) {
                     // fp32 throughout, arranged so that no step cancels:
                     //   lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S  (M - z_t exact),
@@ -897,8 +910,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const float zt = bad ? __int_as_float(0x7fc00000) : ztf;
                     const float lnS = (S == 0.f) ? -INFINITY : logf(S);
                     const float d = (M - zt) + lnS;
-                    const float nll = (d > 0.f) ? d + log1pf(expf(-d)) : log1pf(expf(d));
-                    const float sp_neg = (d > 0.f) ? log1pf(expf(-d)) : -d + log1pf(expf(d));  // softplus(-d)
+                    // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|): one exp, one log1p
+                    const float l1p = log1pf(expf(-fabsf(d)));
+                    const float nll = fmaxf(d, 0.f) + l1p;
+                    const float sp_neg = fmaxf(-d, 0.f) + l1p;   // softplus(-d)
                     float lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
                     if (isnan(d)) lse = d;
                     const float pt = expf(-nll);
@@ -927,15 +942,17 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
                     const float lseL = lse * kLog2e;
                     const float lseL_err = fmaf(lse, kLog2e, -lseL);
-                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2f(fabsf(a)));
+                    // (a - a) keeps a NaN coefficient (an infinite lse) a NaN
+                    const float log2_a = a_fixed ? log2_a_fixed + (a - a) : log2f(fabsf(a));
+                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2_a);
                     cf.neg = a < 0.f;
                     cf.lseL = lseL;
                     const float lu = lse + dlu;
                     const float luL = lu * kLog2e;
                     cf.luL = luL;
                     cf.a = a;
-                    cf.b = s * p.w_kl;
-                    cf.cq = (cf.b > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2f(cf.b)) : INFINITY;
+                    cf.b = b_kl;
+                    cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;
                     cf.gt = (s * p.w_ce + c_r) * tg + s * (zc + p.w_kl) * pt;
                     *coef = cf;
                     if (rank == 0) {

@@ -329,17 +329,15 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 //
 // A cluster of C CTAs owns one row at a time; CTA k of the cluster owns the
 // columns [k*slice, (k+1)*slice).  Each CTA stages its slice (and the teacher
-// slice) in shared memory with one bulk copy per row, then
+// slice) in shared memory with one bulk copy per row, nbuf rows ahead, then
 //   pass A: maximum over its non-target columns (packed bf16x2 max),
 //   pass B: sum of 2^((z - m) log2 e) over non-target columns, relative to
 //           the CTA maximum (+ teacher max, sum and cross term),
-// hands the buffer to the bulk copy of the row nbuf iterations ahead,
-// publishes one record per CTA into every peer's shared memory, and one warp
-// merges the cluster's records in rank order into the row's fp32 scalars.
-// Pass C then writes the gradient of the slice, reading the slice again from
-// global memory, where the bulk copy has just left it in L2: the next row's
-// copy overlaps the record exchange and pass C.  DRAM sees the row read once
-// and the gradient written once.
+// publishes one record per CTA, synchronises the cluster, and one warp reads
+// every CTA's record through distributed shared memory, merges them in rank
+// order and forms the row's scalars in double precision.  Pass C then writes
+// the gradient of the slice from the staged copy.  The row is read from HBM
+// once and the gradient written once.
 //
 // Rows are handed out dynamically: rank 0 of each cluster claims the row for
 // a later iteration from a global counter and passes it to its peers in its
@@ -352,7 +350,7 @@ struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
     float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
     float zt;           // target logit (on the CTA that owns the target column)
-    int next_row;       // rank 0: row for iteration i + nbuf + 1
+    int next_row;       // rank 0: row for iteration i + nbuf
     int next_t;         // rank 0: its target, or -100 when the row is inactive
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
     float pad0, pad1, pad2;
@@ -505,8 +503,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     using IO = Vec<BF16>;
     constexpr int VN = IO::N;
     constexpr int ESZ = IO::ESZ;
-    // pass C: vectors each thread loads before it uses them (register budget)
-    constexpr int kBatch = KL ? (NT >= 512 ? 1 : 2) : 2;
     constexpr int NW = NT / 32;
     static_assert(NW <= 32, "at most 32 warps");
 
@@ -549,8 +545,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         mbar_init(smem_addr(&rbar[0]), 1);
         mbar_init(smem_addr(&rbar[1]), 1);
         for (int k = 0; k < 4; ++k) {
-            rowq[k] = (k <= nbuf) ? cid + k * G : 0x7fffffff;
-            tq[k] = (k <= nbuf && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
+            rowq[k] = (k < nbuf) ? cid + k * G : 0x7fffffff;
+            tq[k] = (k < nbuf && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
         }
         fence_mbar_init();
     }
@@ -574,7 +570,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     };
 
     if (tid == 0)
-        for (int k = 0; k < nbuf; ++k)
+        for (int k = 0; k < nbuf - 1; ++k)
             if (rowq[k] < p.T) issue(rowq[k], tq[k], k);
 
     bool failed = false;
@@ -583,7 +579,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         if (r >= p.T) break;
         __syncthreads();   // buffers, scratch and coefficients of the previous row are free
         int claim_row = 0;
-        if (tid == 0 && rank == 0) claim_row = (nbuf + 1) * G + atomicAdd(p.ws.row_counter, 1);
+        if (tid == 0) {
+            const int j = (i + nbuf - 1) & 3;
+            if (rowq[j] < p.T) issue(rowq[j], tq[j], (i + nbuf - 1) % nbuf);
+            if (rank == 0) claim_row = nbuf * G + atomicAdd(p.ws.row_counter, 1);
+        }
         const int b = i % nbuf;
         const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
 
@@ -781,13 +781,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
         }
         __syncthreads();
-
-        // the staged slice is no longer read: stage the row nbuf iterations ahead
-        // into this buffer (every thread has passed this buffer's wait)
-        if (tid == 0) {
-            const int j = (i + nbuf) & 3;
-            if (rowq[j] < p.T) issue(rowq[j], tq[j], b);
-        }
 
         // ---- publish this CTA's record
         if (warp == 0) {
@@ -992,8 +985,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 if (p.kl_out) p.kl_out[r] = 0.f;
             }
             if (lane == 0) {
-                rowq[(i + nbuf + 1) & 3] = next_row;
-                tq[(i + nbuf + 1) & 3] = next_t;
+                rowq[(i + nbuf) & 3] = next_row;
+                tq[(i + nbuf) & 3] = next_t;
             }
         }
         __syncthreads();
@@ -1010,120 +1003,81 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 continue;
             }
             const RowCoef cf = *coef;
-            // The slice is read again from global memory (the bulk copy of this
-            // row left it in L2): the shared buffer already holds the next row.
-            // Each thread loads kBatch vectors before it computes and stores them.
-            const unsigned char* gz = static_cast<const unsigned char*>(p.logits) + row_off + static_cast<size_t>(e0) * ESZ;
-            const unsigned char* gu = KL ? static_cast<const unsigned char*>(p.teacher) + row_off + static_cast<size_t>(e0) * ESZ
-                                         : nullptr;
             if (KL && cf.a > 0.f && cf.b > 0.f) {
                 // g_j = 2^(z_j log2e - cz) - 2^(u_j log2e - cq): both coefficients in the exponents
                 const uint64_t L2 = f2_pack(kLog2e, kLog2e);
                 const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
                 const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
                 const uint64_t neg1 = f2_pack(-1.f, -1.f);
-                for (int v0 = tid; v0 < nvec; v0 += kBatch * NT) {
-                    uint4 qz[kBatch], qw[kBatch];
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    const uint4 q = lds128(bz + v * 16);
+                    const uint4 qu = lds128(bu + v * 16);
+                    float gv[VN];
 #pragma unroll
-                    for (int b2 = 0; b2 < kBatch; ++b2) {
-                        const int v = v0 + b2 * NT;
-                        if (v < nvec) {
-                            qz[b2] = ldg128(gz + static_cast<size_t>(v) * 16);
-                            qw[b2] = ldg128(gu + static_cast<size_t>(v) * 16);
+                    for (int k = 0; k < VN / 2; ++k) {
+                        float a0, a1, b0, b1;
+                        f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
+                        f2_unpack(f2_fma(IO::pair(qu, k), L2, ncq), b0, b1);
+                        const uint64_t bq = f2_pack(ex2(b0), ex2(b1));
+                        const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
+                        float g0, g1;
+                        f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
+                        if (v == vt) {
+                            float q0, q1;
+                            f2_unpack(bq, q0, q1);
+                            if (2 * k == kt) g0 = cf.gt - q0;
+                            if (2 * k + 1 == kt) g1 = cf.gt - q1;
                         }
+                        gv[2 * k] = g0;
+                        gv[2 * k + 1] = g1;
                     }
-#pragma unroll
-                    for (int b2 = 0; b2 < kBatch; ++b2) {
-                        const int v = v0 + b2 * NT;
-                        if (v >= nvec) break;
-                        float gv[VN];
-#pragma unroll
-                        for (int k = 0; k < VN / 2; ++k) {
-                            float a0, a1, c0f, c1f;
-                            f2_unpack(f2_fma(IO::pair(qz[b2], k), L2, ncz), a0, a1);
-                            f2_unpack(f2_fma(IO::pair(qw[b2], k), L2, ncq), c0f, c1f);
-                            const uint64_t bq = f2_pack(ex2(c0f), ex2(c1f));
-                            const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
-                            float g0, g1;
-                            f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
-                            if (v == vt) {
-                                float q0, q1;
-                                f2_unpack(bq, q0, q1);
-                                if (2 * k == kt) g0 = cf.gt - q0;
-                                if (2 * k + 1 == kt) g1 = cf.gt - q1;
-                            }
-                            gv[2 * k] = g0;
-                            gv[2 * k + 1] = g1;
-                        }
-                        stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
-                    }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                 }
             } else if (KL) {
-                for (int v0 = tid; v0 < nvec; v0 += kBatch * NT) {
-                    uint4 qz[kBatch], qw[kBatch];
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    float x[VN], y[VN], gv[VN], qv[VN];
+                    IO::unpack(lds128(bz + v * 16), x);
+                    IO::unpack(lds128(bu + v * 16), y);
 #pragma unroll
-                    for (int b2 = 0; b2 < kBatch; ++b2) {
-                        const int v = v0 + b2 * NT;
-                        if (v < nvec) {
-                            qz[b2] = ldg128(gz + static_cast<size_t>(v) * 16);
-                            qw[b2] = ldg128(gu + static_cast<size_t>(v) * 16);
-                        }
+                    for (int j = 0; j < VN; ++j) {
+                        qv[j] = cf.b * ex2(fmaf(y[j], kLog2e, -cf.luL));
+                        gv[j] = fmaf(cf.a, ex2(fmaf(x[j], kLog2e, -cf.lseL)), -qv[j]);
                     }
+                    if (v == vt) {
 #pragma unroll
-                    for (int b2 = 0; b2 < kBatch; ++b2) {
-                        const int v = v0 + b2 * NT;
-                        if (v >= nvec) break;
-                        float x[VN], y[VN], gv[VN], qv[VN];
-                        IO::unpack(qz[b2], x);
-                        IO::unpack(qw[b2], y);
-#pragma unroll
-                        for (int j = 0; j < VN; ++j) {
-                            qv[j] = cf.b * ex2(fmaf(y[j], kLog2e, -cf.luL));
-                            gv[j] = fmaf(cf.a, ex2(fmaf(x[j], kLog2e, -cf.lseL)), -qv[j]);
-                        }
-                        if (v == vt) {
-#pragma unroll
-                            for (int j = 0; j < VN; ++j)
-                                if (j == kt) gv[j] = cf.gt - qv[j];
-                        }
-                        stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                        for (int j = 0; j < VN; ++j)
+                            if (j == kt) gv[j] = cf.gt - qv[j];
                     }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                 }
             } else {
                 auto body = [&](auto NEG) {
                     // g_j = (+-) 2^(z_j log2e - cz), two arguments per f32x2 FMA
                     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
                     const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
-                    for (int v0 = tid; v0 < nvec; v0 += kBatch * NT) {
-                        uint4 qz[kBatch];
+#pragma unroll 2
+                    for (int v = tid; v < nvec; v += NT) {
+                        const uint4 q = lds128(bz + v * 16);
+                        float gv[VN];
 #pragma unroll
-                        for (int b2 = 0; b2 < kBatch; ++b2) {
-                            const int v = v0 + b2 * NT;
-                            if (v < nvec) qz[b2] = ldg128(gz + static_cast<size_t>(v) * 16);
+                        for (int k = 0; k < VN / 2; ++k) {
+                            float a0, a1;
+                            f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
+                            gv[2 * k] = ex2(a0);
+                            gv[2 * k + 1] = ex2(a1);
                         }
+                        if (decltype(NEG)::value) {
 #pragma unroll
-                        for (int b2 = 0; b2 < kBatch; ++b2) {
-                            const int v = v0 + b2 * NT;
-                            if (v >= nvec) break;
-                            float gv[VN];
-#pragma unroll
-                            for (int k = 0; k < VN / 2; ++k) {
-                                float a0, a1;
-                                f2_unpack(f2_fma(IO::pair(qz[b2], k), L2, ncz), a0, a1);
-                                gv[2 * k] = ex2(a0);
-                                gv[2 * k + 1] = ex2(a1);
-                            }
-                            if (decltype(NEG)::value) {
-#pragma unroll
-                                for (int j = 0; j < VN; ++j) gv[j] = -gv[j];
-                            }
-                            if (v == vt) {
-#pragma unroll
-                                for (int j = 0; j < VN; ++j)
-                                    if (j == kt) gv[j] = cf.gt;
-                            }
-                            stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                            for (int j = 0; j < VN; ++j) gv[j] = -gv[j];
                         }
+                        if (v == vt) {
+#pragma unroll
+                            for (int j = 0; j < VN; ++j)
+                                if (j == kt) gv[j] = cf.gt;
+                        }
+                        stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
                     }
                 };
                 if (cf.neg) body(BoolConst<true>{});

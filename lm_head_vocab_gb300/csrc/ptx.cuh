@@ -134,18 +134,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
-// 16-byte global load, not kept in L1 (each vector is read once); ordered
-// with the stores around it, since the gradient may overwrite the logits.
-__device__ __forceinline__ uint4 ldg128(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void stg128(void* p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

@@ -76,7 +76,7 @@ struct Vec<true> {
     {
         return fmaxf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
     }
-    // Running packed minimum (spots -inf and NaN teacher logits: NaN propagates).
+    // Running packed minimum (used to spot -inf teacher logits).
     __device__ static __forceinline__ uint32_t min_init() { return 0x7f807f80u; }  // (+inf, +inf)
     __device__ static __forceinline__ uint32_t min_acc(uint32_t acc, const uint4& q)
     {
@@ -84,13 +84,13 @@ struct Vec<true> {
         __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
         __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&q.z);
         __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&q.w);
-        __nv_bfloat162 m = __hmin2_nan(__hmin2_nan(a, b), __hmin2_nan(c, d));
-        __nv_bfloat162 r = __hmin2_nan(m, *reinterpret_cast<__nv_bfloat162*>(&acc));
+        __nv_bfloat162 m = __hmin2(__hmin2(a, b), __hmin2(c, d));
+        __nv_bfloat162 r = __hmin2(m, *reinterpret_cast<__nv_bfloat162*>(&acc));
         return *reinterpret_cast<uint32_t*>(&r);
     }
     __device__ static __forceinline__ float min_final(uint32_t acc)
     {
-        return fmin_nan(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
+        return fminf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
     }
     // Pair k (elements 2k, 2k+1) of a vector as packed fp32.
     __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
@@ -343,17 +343,7 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 // a later iteration from a global counter and passes it to its peers in its
 // record, so clusters that share SMs with others do not set the pace.
 // ======================================================================
-constexpr int kHdrBytes = 3072;
-// Pairs of each 8-element vector whose teacher exponentials take the FMA-pipe
-// polynomial in the distillation passes (B: sums, C: gradient), bf16 only.
-#ifndef LMLOSS_POLY_PAIRS_B
-#define LMLOSS_POLY_PAIRS_B 1
-#endif
-#ifndef LMLOSS_POLY_PAIRS_C
-#define LMLOSS_POLY_PAIRS_C 2
-#endif
-constexpr int kPolyPairsB = LMLOSS_POLY_PAIRS_B;
-constexpr int kPolyPairsC = LMLOSS_POLY_PAIRS_C;   // mbarriers, row queue, cluster records, warp scratch
+constexpr int kHdrBytes = 3072;   // mbarriers, row queue, cluster records, warp scratch
 constexpr int kMaxCluster = 16;
 
 struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
@@ -434,10 +424,7 @@ __device__ __forceinline__ void sums_plain(uint32_t bz, int nvec, int tid, int v
 
 // The same with the teacher slice (guard-free form: no teacher logit is -inf):
 //   su = sum 2^c, c = u log2e - muL,   w = sum 2^c (u - z).
-// With POLY (every c >= -124 in this slice), the teacher exponentials of the
-// first kPolyPairsB pairs of each vector come from f2_exp2_poly on the FMA pipe
-// instead of the special-function unit, which this pass otherwise saturates.
-template <class IO, int NT, bool ENT, bool POLY>
+template <class IO, int NT, bool ENT>
 __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float mL,
                                         float muL, float& s_out, float& su_out, float& w_out, float& b_out)
 {
@@ -466,7 +453,7 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
             const uint64_t ez = f2_pack(e0, e1);
             accz = f2_add(accz, ez);
             if (ENT) accb = f2_fma(ez, argz, accb);
-            const uint64_t eu = (POLY && k < kPolyPairsB) ? f2_exp2_poly(f2_pack(u0, u1)) : f2_pack(ex2(u0), ex2(u1));
+            const uint64_t eu = f2_pack(ex2(u0), ex2(u1));
             accu = f2_add(accu, eu);
             accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
         }
@@ -646,21 +633,21 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
-                if (v != vt) accz = IO::max_acc(accz, q);
+                if (v == vt) {
+                    float x[VN];
+                    IO::unpack(q, x);
+#pragma unroll
+                    for (int j = 0; j < VN; ++j) {
+                        if (j != kt) mx = fmaxf(mx, x[j]);
+                        else slot[0] = x[j];
+                    }
+                } else {
+                    accz = IO::max_acc(accz, q);
+                }
                 if (KL) {
                     const uint4 qu = lds128(bu + v * 16);
                     accu = IO::max_acc(accu, qu);
                     accn = IO::min_acc(accn, qu);
-                }
-            }
-            if (vt >= 0 && vt % NT == tid) {
-                // the vector holding the target: its other columns, and the target logit
-                float x[VN];
-                IO::unpack(lds128(bz + vt * 16), x);
-#pragma unroll
-                for (int j = 0; j < VN; ++j) {
-                    if (j != kt) mx = fmaxf(mx, x[j]);
-                    else slot[0] = x[j];
                 }
             }
             if (tid == NT - 1) {
@@ -673,7 +660,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             mu = fmaxf(mu, y);
-                            un = fmin_nan(un, y);
+                            un = fminf(un, y);
                         }
                     }
                 }
@@ -683,11 +670,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
             if (KL) {
                 mu = fmaxf(mu, IO::max_final(accu));
-                un = fmin_nan(un, IO::min_final(accn));
+                un = fminf(un, IO::min_final(accn));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
-                    un = fmin_nan(un, __shfl_xor_sync(0xffffffffu, un, off));
+                    un = fminf(un, __shfl_xor_sync(0xffffffffu, un, off));
                 }
             }
             if (lane == 0) {
@@ -699,7 +686,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 
         // ---- pass B: sums relative to the CTA maximum
         float m_cta = -INFINITY, mu_cta = -INFINITY;
-        float u_lo = -INFINITY;   // teacher minimum over the slice (NaN if any is NaN)
         if (act && mode != kModeGrad) {
             m_cta = (lane < NW) ? wred[lane] : -INFINITY;
 #pragma unroll
@@ -721,18 +707,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 // with no -inf teacher logit in the slice, e^(u-mu) (u - z) needs no guard
                 float un_cta = (lane < NW) ? wred[160 + lane] : INFINITY;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) un_cta = fmin_nan(un_cta, __shfl_xor_sync(0xffffffffu, un_cta, off));
-                u_lo = un_cta;
+                for (int off = 16; off > 0; off >>= 1) un_cta = fminf(un_cta, __shfl_xor_sync(0xffffffffu, un_cta, off));
                 if (un_cta > -INFINITY) {
-                    // polynomial exponentials need every teacher argument >= -124
-                    const bool poly = BF16 && (un_cta - mu_cta) * kLog2e > -124.f;
-                    if (p.entropy_out) {
-                        if (poly) sums_kl<IO, NT, true, BF16>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                        else sums_kl<IO, NT, true, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                    } else {
-                        if (poly) sums_kl<IO, NT, false, BF16>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                        else sums_kl<IO, NT, false, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                    }
+                    if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
+                    else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
                 } else {
 #pragma unroll 2
                     for (int v = tid; v < nvec; v += NT) {
@@ -1027,50 +1005,35 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const RowCoef cf = *coef;
             if (KL && cf.a > 0.f && cf.b > 0.f) {
                 // g_j = 2^(z_j log2e - cz) - 2^(u_j log2e - cq): both coefficients in the exponents
-                auto kl_body = [&](auto POLY) {
-                    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
-                    const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
-                    const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
-                    const uint64_t neg1 = f2_pack(-1.f, -1.f);
+                const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
+                const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
+                const uint64_t neg1 = f2_pack(-1.f, -1.f);
 #pragma unroll 2
-                    for (int v = tid; v < nvec; v += NT) {
-                        const uint4 q = lds128(bz + v * 16);
-                        const uint4 qu = lds128(bu + v * 16);
-                        float gv[VN];
+                for (int v = tid; v < nvec; v += NT) {
+                    const uint4 q = lds128(bz + v * 16);
+                    const uint4 qu = lds128(bu + v * 16);
+                    float gv[VN];
 #pragma unroll
-                        for (int k = 0; k < VN / 2; ++k) {
-                            float a0, a1;
-                            f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
-                            const uint64_t argq = f2_fma(IO::pair(qu, k), L2, ncq);
-                            uint64_t bq;
-                            if (decltype(POLY)::value && k < kPolyPairsC) {
-                                bq = f2_exp2_poly(argq);
-                            } else {
-                                float b0, b1;
-                                f2_unpack(argq, b0, b1);
-                                bq = f2_pack(ex2(b0), ex2(b1));
-                            }
-                            const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
-                            float g0, g1;
-                            f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
-                            if (v == vt) {
-                                float q0, q1;
-                                f2_unpack(bq, q0, q1);
-                                if (2 * k == kt) g0 = cf.gt - q0;
-                                if (2 * k + 1 == kt) g1 = cf.gt - q1;
-                            }
-                            gv[2 * k] = g0;
-                            gv[2 * k + 1] = g1;
+                    for (int k = 0; k < VN / 2; ++k) {
+                        float a0, a1, b0, b1;
+                        f2_unpack(f2_fma(IO::pair(q, k), L2, ncz), a0, a1);
+                        f2_unpack(f2_fma(IO::pair(qu, k), L2, ncq), b0, b1);
+                        const uint64_t bq = f2_pack(ex2(b0), ex2(b1));
+                        const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
+                        float g0, g1;
+                        f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
+                        if (v == vt) {
+                            float q0, q1;
+                            f2_unpack(bq, q0, q1);
+                            if (2 * k == kt) g0 = cf.gt - q0;
+                            if (2 * k + 1 == kt) g1 = cf.gt - q1;
                         }
-                        stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                        gv[2 * k] = g0;
+                        gv[2 * k + 1] = g1;
                     }
-                };
-                // the polynomial needs every teacher argument in [-124, 126]; the
-                // slice's teacher minimum (not NaN, not -inf) and maximum bound them
-                const bool poly = BF16 && u_lo > -INFINITY && fmaf(u_lo, kLog2e, -cf.cq) > -124.f &&
-                                  fmaf(mu_cta, kLog2e, -cf.cq) < 126.f;
-                if (poly) kl_body(BoolConst<BF16>{});
-                else kl_body(BoolConst<false>{});
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                }
             } else if (KL) {
 #pragma unroll 2
                 for (int v = tid; v < nvec; v += NT) {

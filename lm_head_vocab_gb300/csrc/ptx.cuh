@@ -170,46 +170,12 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 }
 
 // ---------------------------------------------------------------- math
-// Minimum that is NaN when either input is NaN.
-__device__ __forceinline__ float fmin_nan(float a, float b)
-{
-    float r;
-    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 // 2^x on the special-function unit (flushes results below 2^-126 to 0).
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x for a packed pair on the FMA pipe, so that part of a pass's exponentials
-// leave the special-function unit.  Valid for x in [-125, 128): x = n + f with
-// n = rint(x) (adding 1.5 * 2^23 rounds to the nearest integer) and
-// f = x - n in [-1/2, 1/2] exactly; 2^f from a degree-5 polynomial fitted by
-// Remez exchange on the relative error (coefficients from exp2_poly.py, fp32
-// evaluation within 2.1e-7 relative); n is then added to the exponent field.
-__device__ __forceinline__ uint64_t f2_exp2_poly(uint64_t x)
-{
-    const uint64_t magic = f2_pack(12582912.0f, 12582912.0f);
-    const uint64_t t = f2_add(x, magic);
-    const uint64_t n = f2_add(t, f2_pack(-12582912.0f, -12582912.0f));
-    const uint64_t f = f2_fma(n, f2_pack(-1.0f, -1.0f), x);
-    uint64_t q = f2_fma(f, f2_pack(1.327647245e-03f, 1.327647245e-03f), f2_pack(9.675540961e-03f, 9.675540961e-03f));
-    q = f2_fma(q, f, f2_pack(5.550713092e-02f, 5.550713092e-02f));
-    q = f2_fma(q, f, f2_pack(2.402212024e-01f, 2.402212024e-01f));
-    q = f2_fma(q, f, f2_pack(6.931469440e-01f, 6.931469440e-01f));
-    q = f2_fma(q, f, f2_pack(1.000000119e+00f, 1.000000119e+00f));
-    float q0, q1, t0, t1;
-    f2_unpack(q, q0, q1);
-    f2_unpack(t, t0, t1);
-    // the low bits of t hold n (two's complement): shifted into the exponent field
-    const float r0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-    const float r1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
-    return f2_pack(r0, r1);
 }
 
 }  // namespace lmloss

@@ -306,3 +306,53 @@ def test_forward_only_with_teacher(dev, handle):
     torch.cuda.synchronize()
     assert handle.device_error() == 0
     compare_all(case, out, R, None, "forward only with teacher")
+
+
+def _kl_problem(dev, handle, z, u, t):
+    """bf16 student and teacher, KL weight 0.5, z-loss 1e-3."""
+    zb = workloads.bf16_round(z.astype(np.float32))
+    ub = workloads.bf16_round(u.astype(np.float32))
+    P = oracle.Problem(logits=zb, V=z.shape[1], targets=t, teacher=ub, kl_weight=0.5, z_alpha=1e-3)
+    out = handle.forward_backward(to_device(zb, dev), torch.from_numpy(t).to(dev),
+                                  teacher_logits=to_device(ub, dev), kl_weight=0.5, z_alpha=1e-3,
+                                  grad="new", want=("logp", "lse", "kl", "count"))
+    torch.cuda.synchronize()
+    return P, out
+
+
+@pytest.mark.parametrize("spread", [30.0, 140.0])
+def test_kl_teacher_range(dev, handle, spread):
+    """Teacher rows whose logits span `spread` nats (140: the smallest teacher
+    probabilities underflow fp32 and flush to 0 in the exponentials)."""
+    rng = np.random.default_rng(int(spread))
+    T, V = 24, 40000
+    z = rng.normal(0, 2, size=(T, V))
+    u = z + rng.normal(0, 1, size=(T, V))
+    cols = rng.integers(0, V, size=(T, 50))
+    for r in range(T):
+        u[r, cols[r]] = u[r].max() - spread
+    t = rng.integers(0, V, size=T)
+    P, out = _kl_problem(dev, handle, z, u, t)
+    assert handle.device_error() == 0
+    R, g_ref, scale = oracle.forward_backward(P, with_scale=True)
+    assert rel(float(out.loss[0]), R.total) <= 1e-5 and rel(float(out.loss[3]), R.kl_loss) <= 1e-5
+    np.testing.assert_allclose(out.kl.cpu().numpy(), R.kl, rtol=1e-4, atol=2e-6)
+    check_grad(grad_to_f64(out.grad), g_ref, True, f"teacher spread {spread}", scale)
+
+
+def test_kl_teacher_nan_propagates(dev, handle):
+    """A NaN teacher logit makes that row's KL and gradient NaN, and no other row's."""
+    rng = np.random.default_rng(9)
+    T, V = 6, 3000
+    z = rng.normal(0, 2, size=(T, V))
+    u = z + rng.normal(0, 1, size=(T, V))
+    u[2, 1234] = np.nan
+    t = rng.integers(0, V, size=T)
+    P, out = _kl_problem(dev, handle, z, u, t)
+    assert handle.device_error() == 0
+    g = out.grad.float().cpu().numpy()
+    kl = out.kl.cpu().numpy()
+    assert np.isnan(kl[2]) and np.all(np.isnan(g[2]))
+    others = [r for r in range(T) if r != 2]
+    assert np.all(np.isfinite(kl[others])) and np.all(np.isfinite(g[others]))
+    assert np.isnan(float(out.loss[0]))

@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
-    ap.add_argument("--nbuf", type=int, default=0)
+    ap.add_argument("--chunks", type=int, default=0)
     ap.add_argument("--rows", type=int, default=0, help="profiling only: fewer rows than the workload")
     return ap.parse_args()
 
@@ -283,8 +283,8 @@ def run_ours(args):
     tg = torch.from_numpy(targets).to(dev)
     mk = None if mask is None else torch.from_numpy(mask).to(dev)
     h = LMLoss(dev.index, max_T=w.T, max_segments=1)
-    if args.cluster or args.threads or args.nbuf:
-        h.set_launch_config(args.cluster, args.threads, args.nbuf)
+    if args.cluster or args.threads or args.chunks:
+        h.set_launch_config(args.cluster, args.threads, args.chunks)
     grad_mode = "inplace" if w.in_place else "new"
     a, out, keep = h.build_args(logits, tg, mk, teacher_logits=teacher, grad=grad_mode, want=(), **kw)
     stream = torch.cuda.current_stream(dev)
@@ -389,7 +389,7 @@ def run_ours(args):
                 "reduction": kw["reduction"], "grad": grad_mode,
                 "l2": f"inputs larger than L2 ({w.T * w.V * w.elem_bytes / 1e9:.2f} GB of logits per step)",
                 "parallelism": f"rows x{world}" if world > 1 else "single GPU",
-                "launch": {k: info[k] for k in ("cluster", "threads", "nbuf", "grid", "smem_bytes")},
+                "launch": {k: info[k] for k in ("cluster", "threads", "chunks", "grid", "smem_bytes")},
             },
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

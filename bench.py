@@ -163,11 +163,10 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ inputs
 def make_problem(w, rank: int, world: int):
-    """This rank's rows of workload w (a batch world x T rows tall when world > 1)
-    and the global active-row count, computed on the host from the seeds."""
-    if w.has_gspo:
-        raise SystemExit("bench: the GSPO workload needs oracle log-probs for its inputs; "
-                         "benchmark it through tests, not here")
+    """This rank's rows of workload w (a batch world x T rows tall when world > 1),
+    the global active-row count, and for GSPO this rank's segments (renumbered
+    from 0; packed rows never straddle ranks) with their advantages and the
+    rows' old-log-prob noise, all computed on the host from the seeds."""
     wg = w if world == 1 else w.with_shape(w.T * world, w.V)
     r0 = rank * w.T
     targets = wg.targets()[r0:r0 + w.T].copy()
@@ -187,11 +186,23 @@ def make_problem(w, rank: int, world: int):
             n = min(chunk, w.T - a)
             u[a:a + n] = wg.teacher_rows(r0 + a, n, x[a:a + n])
     n_active_global = wg.n_active()
-    return w, x, u, targets, mask, n_active_global
+    gspo = None
+    if w.has_gspo:
+        if w.T % w.packed_len:
+            raise SystemExit("bench: GSPO rows per rank must be whole packed rows")
+        seg_all, _, adv_all = wg.segments()
+        seg = seg_all[r0:r0 + w.T].copy()
+        s0, s1 = int(seg.min()), int(seg.max()) + 1
+        seg -= s0
+        gspo = dict(seg=seg.astype(np.int32), S=s1 - s0, adv=adv_all[s0:s1].copy(),
+                    noise=wg.old_logp_noise()[r0:r0 + w.T].astype(np.float32))
+    return w, x, u, targets, mask, n_active_global, gspo
 
 
 def call_kwargs(w, world, n_active_global):
     kw = dict(ce_weight=w.ce_weight, z_alpha=w.z_alpha, kl_weight=w.kl_weight, temperature=w.temperature)
+    if w.has_gspo:
+        kw.update(clip_eps_low=w.clip_eps_low, clip_eps_high=w.clip_eps_high)
     if world > 1 or w.reduction == "sum_active":
         kw.update(reduction="sum", denominator=float(n_active_global))
     else:
@@ -200,9 +211,11 @@ def call_kwargs(w, world, n_active_global):
 
 
 # ------------------------------------------------------------ oracle timing
-def oracle_sample_time(w, x, u, targets, mask, seconds: float):
+def oracle_sample_time(w, x, u, targets, mask, seconds: float, gspo=None):
     """Time the fp64 oracle (forward + gradient) on the first R rows, R sized
-    for about `seconds` of host work.  Returns (elements/s, cores, description)."""
+    for about `seconds` of host work.  Returns (elements/s, cores, description).
+    With GSPO the old log-probs are the seeded noise around -10: the oracle's
+    work (forward, seam, gradient) does not depend on their values."""
     import oracle
     cores = os.cpu_count() or 1
 
@@ -211,6 +224,12 @@ def oracle_sample_time(w, x, u, targets, mask, seconds: float):
                            loss_mask=None if mask is None else mask[:rows], ce_weight=w.ce_weight,
                            z_alpha=w.z_alpha, teacher=None if u is None else u[:rows],
                            kl_weight=w.kl_weight, temperature=w.temperature)
+        if gspo is not None:
+            P.segment_ids = gspo["seg"][:rows]
+            P.num_segments = gspo["S"]
+            P.advantages = gspo["adv"]
+            P.old_logprobs = (gspo["noise"][:rows] - 10.0).astype(np.float32)
+            P.clip_eps_low, P.clip_eps_high = w.clip_eps_low, w.clip_eps_high
         t0 = time.perf_counter()
         oracle.forward_backward(P, nthreads=cores)
         return time.perf_counter() - t0
@@ -229,10 +248,10 @@ def run_reference(args):
     if rank != 0:
         return
     import workloads
-    w, x, u, targets, mask, n_glob = make_problem(workloads.get(args.workload), 0, 1)
+    w, x, u, targets, mask, n_glob, gspo = make_problem(workloads.get(args.workload), 0, 1)
     per_step = []
     for i in range(args.warmup + args.steps):
-        v, cores, desc = oracle_sample_time(w, x, u, targets, mask, args.cpu_seconds / 4)
+        v, cores, desc = oracle_sample_time(w, x, u, targets, mask, args.cpu_seconds / 4, gspo)
         if i >= args.warmup:
             per_step.append(v)
     value = statistics.median(per_step)
@@ -268,7 +287,7 @@ def run_ours(args):
     wl = workloads.get(args.workload)
     if args.rows:
         wl = wl.with_shape(args.rows, wl.V)
-    w, x, u, targets, mask, n_glob = make_problem(wl, rank, world)
+    w, x, u, targets, mask, n_glob, gspo = make_problem(wl, rank, world)
     kw = call_kwargs(w, world, n_glob)
 
     def to_dev(a):
@@ -282,11 +301,22 @@ def run_ours(args):
     teacher = to_dev(u)
     tg = torch.from_numpy(targets).to(dev)
     mk = None if mask is None else torch.from_numpy(mask).to(dev)
-    h = LMLoss(dev.index, max_T=w.T, max_segments=1)
+    h = LMLoss(dev.index, max_T=w.T, max_segments=gspo["S"] if gspo else 1)
     if args.cluster or args.threads or args.chunks:
         h.set_launch_config(args.cluster, args.threads, args.chunks)
     grad_mode = "inplace" if w.in_place else "new"
-    a, out, keep = h.build_args(logits, tg, mk, teacher_logits=teacher, grad=grad_mode, want=(), **kw)
+    gkw = {}
+    if gspo is not None:
+        # old log-probs for a timing run: this path's own log-probs plus the
+        # seeded noise (the policy term's values do not change the work)
+        a0, o0, k0 = h.build_args(logits, tg, mk, grad=None, want=("logp",))
+        h.call(a0)
+        torch.cuda.synchronize(dev)
+        old = (o0.logp + torch.from_numpy(gspo["noise"]).to(dev)).contiguous()
+        del a0, o0, k0
+        gkw = dict(segment_ids=torch.from_numpy(gspo["seg"]).to(dev), num_segments=gspo["S"],
+                   advantages=torch.from_numpy(gspo["adv"]).to(dev), old_logprobs=old)
+    a, out, keep = h.build_args(logits, tg, mk, teacher_logits=teacher, grad=grad_mode, want=(), **gkw, **kw)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -344,6 +374,13 @@ def run_ours(args):
         du = None if teacher is None else teacher.view(torch.int16)
         h2d = hx.numel() * hx.element_size() + ht.numel() * 8 + (0 if hu is None else hu.numel() * 2) \
             + (0 if hm is None else hm.numel())
+        hg = None
+        if gspo is not None:
+            # the policy inputs travel too: segment ids, advantages, old log-probs
+            hg = [(gkw["segment_ids"], torch.from_numpy(gspo["seg"]).pin_memory()),
+                  (gkw["advantages"], torch.from_numpy(gspo["adv"]).pin_memory()),
+                  (gkw["old_logprobs"], gkw["old_logprobs"].cpu().pin_memory())]
+            h2d += sum(hs.numel() * hs.element_size() for _, hs in hg)
 
         def e2e_step():
             dl.copy_(hx, non_blocking=True)
@@ -352,6 +389,9 @@ def run_ours(args):
                 du.copy_(hu, non_blocking=True)
             if hm is not None:
                 mk.copy_(hm, non_blocking=True)
+            if hg is not None:
+                for dst, src in hg:
+                    dst.copy_(src, non_blocking=True)
             h.call(a, stream)
             hloss.copy_(out.loss, non_blocking=True)
 
@@ -376,7 +416,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, cores, desc = oracle_sample_time(w, x, u, targets, mask, args.cpu_seconds)
+        v, cores, desc = oracle_sample_time(w, x, u, targets, mask, args.cpu_seconds, gspo)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
     if rank == 0:

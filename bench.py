@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--threads", type=int, default=0)
-    ap.add_argument("--chunks", type=int, default=0)
+    ap.add_argument("--nbuf", type=int, default=0)
     ap.add_argument("--rows", type=int, default=0, help="profiling only: fewer rows than the workload")
     return ap.parse_args()
 
@@ -285,6 +285,7 @@ def run_ours(args):
 
     import workloads
     wl = workloads.get(args.workload)
+    wl_full_T = wl.T
     if args.rows:
         wl = wl.with_shape(args.rows, wl.V)
     w, x, u, targets, mask, n_glob, gspo = make_problem(wl, rank, world)
@@ -302,8 +303,8 @@ def run_ours(args):
     tg = torch.from_numpy(targets).to(dev)
     mk = None if mask is None else torch.from_numpy(mask).to(dev)
     h = LMLoss(dev.index, max_T=w.T, max_segments=gspo["S"] if gspo else 1)
-    if args.cluster or args.threads or args.chunks:
-        h.set_launch_config(args.cluster, args.threads, args.chunks)
+    if args.cluster or args.threads or args.nbuf:
+        h.set_launch_config(args.cluster, args.threads, args.nbuf)
     grad_mode = "inplace" if w.in_place else "new"
     gkw = {}
     if gspo is not None:
@@ -360,6 +361,11 @@ def run_ours(args):
     value = world * elems_rank / (step_ms / 1e3)
     alg_bytes = w.algorithmic_bytes()
     peak, peak_kind = read_peaks()
+    # the recorded traffic is per launch over the workload's full rows; a --rows
+    # run moves the same bytes per row
+    traffic = read_traffic(f"fused_kernel_{w.name}")
+    if traffic is not None and w.T != wl_full_T:
+        traffic = int(round(traffic * w.T / wl_full_T))
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
 
     # ---- end to end through the C ABI with host buffers
@@ -429,11 +435,11 @@ def run_ours(args):
                 "reduction": kw["reduction"], "grad": grad_mode,
                 "l2": f"inputs larger than L2 ({w.T * w.V * w.elem_bytes / 1e9:.2f} GB of logits per step)",
                 "parallelism": f"rows x{world}" if world > 1 else "single GPU",
-                "launch": {k: info[k] for k in ("cluster", "threads", "chunks", "grid", "smem_bytes")},
+                "launch": {k: info[k] for k in ("cluster", "threads", "nbuf", "grid", "smem_bytes")},
             },
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": read_traffic(f"fused_kernel_{w.name}"),
+                         "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s", "kernel_ms": kern_ms,
                          "algorithmic_bytes": alg_bytes},

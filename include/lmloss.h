@@ -126,7 +126,7 @@ typedef struct {
     int32_t path;                /* 0 fused single-read, 1 stats-only, 2 GSPO three-phase  */
     int32_t cluster;             /* CTAs per row in the fused kernel                       */
     int32_t threads;             /* threads per CTA of the main kernel                     */
-    int32_t chunks;              /* pieces each staged slice is copied in (1 or 2)         */
+    int32_t nbuf;                /* staged rows per CTA in the fused kernel                */
     int32_t grid;                /* CTAs of the main kernel                                */
     int32_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel       */
     int32_t reserved;
@@ -174,11 +174,10 @@ lmloss_status lmloss_get_device_error(lmloss_handle handle);
 const char* lmloss_status_string(lmloss_status status);
 
 /* Override the fused kernel's launch shape: cluster size (1..16), threads per
- * CTA (128, 256, 512 or 1024) and the pieces each CTA's staged slice is copied
- * in (1, or 2: the first piece of the next row loads while the gradient of the
- * second is written).  0 keeps the automatic choice.  Shapes that do not fit
- * are rejected at the next call with LMLOSS_ERR_UNSUPPORTED. */
-lmloss_status lmloss_set_launch_config(lmloss_handle handle, int cluster, int threads, int chunks);
+ * CTA (128, 256, 384, 512 or 1024) and rows staged per CTA (1 or 2).  0 keeps
+ * the automatic choice.  Shapes that do not fit are rejected at the next call
+ * with LMLOSS_ERR_UNSUPPORTED. */
+lmloss_status lmloss_set_launch_config(lmloss_handle handle, int cluster, int threads, int nbuf);
 
 /* When enabled (which also resets the record), each call records a pair of
  * CUDA events on its stream around its main kernel(s), up to 4096 calls.

@@ -95,7 +95,7 @@ class lmloss_args(ctypes.Structure):
 
 class lmloss_call_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("launches", "path", "cluster", "threads", "chunks", "grid", "smem_bytes", "reserved")]
+                ("launches", "path", "cluster", "threads", "nbuf", "grid", "smem_bytes", "reserved")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -175,8 +175,8 @@ def lmloss_get_device_error(handle) -> int:
     return load().lmloss_get_device_error(handle)
 
 
-def lmloss_set_launch_config(handle, cluster: int = 0, threads: int = 0, chunks: int = 0) -> int:
-    return load().lmloss_set_launch_config(handle, cluster, threads, chunks)
+def lmloss_set_launch_config(handle, cluster: int = 0, threads: int = 0, nbuf: int = 0) -> int:
+    return load().lmloss_set_launch_config(handle, cluster, threads, nbuf)
 
 
 def lmloss_set_timing(handle, enable: bool) -> int:

@@ -224,7 +224,7 @@ struct CallParams {
     int mode;               // kModeFused, kModeStats or kModeGrad
     int cluster;
     int64_t slice;          // elements per CTA of a row (multiple of the vector width)
-    int chunks;             // 1: the slice is copied in one piece; 2: in two, see fused_kernel
+    int nbuf;
     uint32_t buf_bytes;     // bytes of one staged slice
 };
 
@@ -329,37 +329,28 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 //
 // A cluster of C CTAs owns one row at a time; CTA k of the cluster owns the
 // columns [k*slice, (k+1)*slice).  Each CTA stages its slice (and the teacher
-// slice) in shared memory with bulk copies, then
+// slice) in shared memory with one bulk copy per row, nbuf rows ahead, then
 //   pass A: maximum over its non-target columns (packed bf16x2 max),
 //   pass B: sum of 2^((z - m) log2 e) over non-target columns, relative to
 //           the CTA maximum (+ teacher max, sum and cross term),
 // publishes one record per CTA, synchronises the cluster, and one warp reads
 // every CTA's record through distributed shared memory, merges them in rank
-// order and forms the row's fp32 scalars.  Pass C then writes the gradient of
-// the slice from the staged copy.  The row is read from HBM once and the
-// gradient written once.
-//
-// With two chunks, the slice is copied as two pieces with a barrier each: the
-// first piece of the next row is copied as soon as pass C is done with the
-// first piece of this one (while pass C writes the second), and pass A starts
-// on the first piece while the second is still arriving.  Each piece of row
-// i+1 is issued only after a CTA barrier that every thread reaches after its
-// wait for that piece of row i and its last read of it, so no barrier can
-// complete a phase that a thread has not yet waited for.
+// order and forms the row's scalars in double precision.  Pass C then writes
+// the gradient of the slice from the staged copy.  The row is read from HBM
+// once and the gradient written once.
 //
 // Rows are handed out dynamically: rank 0 of each cluster claims the row for
 // a later iteration from a global counter and passes it to its peers in its
 // record, so clusters that share SMs with others do not set the pace.
 // ======================================================================
-constexpr int kHdrBytes = 3072;
-constexpr int kDefaultChunks = 2;   // pieces per staged slice unless the caller sets it   // mbarriers, row queue, cluster records, warp scratch
+constexpr int kHdrBytes = 3072;   // mbarriers, row queue, cluster records, warp scratch
 constexpr int kMaxCluster = 16;
 
 struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
     float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
     float zt;           // target logit (on the CTA that owns the target column)
-    int next_row;       // rank 0: row for iteration i + 1
+    int next_row;       // rank 0: row for iteration i + nbuf
     int next_t;         // rank 0: its target, or -100 when the row is inactive
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
     float pad0, pad1, pad2;
@@ -502,10 +493,9 @@ __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int
 }
 
 // Occupancy: without a teacher, shared memory admits 1024 threads per SM at the
-// default shape; with one, registers are capped so that three CTAs of up to
-// 256 threads (two of 512) fit, as slices small enough for three allow.
+// default shape; with one, two CTAs share an SM, so registers are capped to fit two.
 template <bool KL, int NT>
-constexpr int fused_min_blocks() { return NT >= 1024 ? 1 : (KL ? (NT >= 512 ? 2 : 768 / NT) : 1024 / NT); }
+constexpr int fused_min_blocks() { return NT >= 1024 ? 1 : (KL ? 2 : 1024 / NT); }
 
 template <bool BF16, bool KL, int NT>
 __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel(const CallParams p)
@@ -517,7 +507,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     static_assert(NW <= 32, "at most 32 warps");
 
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);                  // [2] the slice's two pieces
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);                  // [2] staged-row copies
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + 16);             // [2] cluster records, by row parity
     int* rowq = reinterpret_cast<int*>(smem + 32);                       // [4] row of iteration i (i & 3)
     int* tq = reinterpret_cast<int*>(smem + 48);                         // [4] its target (-100: inactive)
@@ -535,7 +525,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     const int G = static_cast<int>(gridDim.x) / C;
     const int64_t c0 = min(p.V, static_cast<int64_t>(rank) * p.slice);
     const int64_t c1 = min(p.V, c0 + p.slice);
-    const int chunks = p.chunks;
+    const int nbuf = p.nbuf;
     const float s_tok = token_scale(p);
     // Kernel-wide constants of the row coefficients: b = s w_kl and, when no
     // per-row term enters it (no z-loss, no policy term), a = s (w_ce + w_kl).
@@ -545,47 +535,43 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     const float log2_a_fixed = log2f(fabsf(s_tok * (p.w_ce + p.w_kl)));
     const int mode = p.mode;
 
-    auto buf_addr = [&](int a) -> uint32_t { return smem_addr(bufs + static_cast<size_t>(a) * p.buf_bytes); };
-    auto bar_addr = [&](int c) -> uint32_t { return smem_addr(&mbar[c]); };
-    // interior vectors in piece 0 (a multiple of NT, so each thread's vectors
-    // v = tid + k NT split cleanly between the pieces)
-    auto split = [&](int nv) -> int { return chunks == 2 ? (nv / 2) / NT * NT : nv; };
+    auto buf_addr = [&](int b, int a) -> uint32_t {
+        return smem_addr(bufs + (static_cast<size_t>(b) * (KL ? 2 : 1) + a) * p.buf_bytes);
+    };
+    auto bar_addr = [&](int b) -> uint32_t { return smem_addr(&mbar[b]); };
 
     if (tid == 0) {
-        mbar_init(bar_addr(0), 1);
-        mbar_init(bar_addr(1), 1);
+        for (int b = 0; b < nbuf; ++b) mbar_init(bar_addr(b), 1);
         mbar_init(smem_addr(&rbar[0]), 1);
         mbar_init(smem_addr(&rbar[1]), 1);
         for (int k = 0; k < 4; ++k) {
-            rowq[k] = (k == 0) ? cid : 0x7fffffff;
-            tq[k] = (k == 0 && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
+            rowq[k] = (k < nbuf) ? cid + k * G : 0x7fffffff;
+            tq[k] = (k < nbuf && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
         }
         fence_mbar_init();
     }
     cluster_sync_all();   // every peer's record barriers exist before anyone pushes
 
-    // Producer side (thread 0): stage piece c of row rr's slice; an inactive
-    // row or an empty piece only arrives on the piece's barrier.
-    auto issue = [&](int64_t rr, int tt, int c) {
+    // Producer side (thread 0): stage row rr's slice into buffer b.
+    auto issue = [&](int64_t rr, int tt, int b) {
         const bool act = tt != -100;
         int64_t e0, e1;
         row_interior<ESZ>(p.logits, rr, p.ld, c0, c1, e0, e1);
-        const int nv = static_cast<int>((e1 - e0) / VN);
-        const int nv0 = split(nv);
-        const int vb = c ? nv0 : 0, ve = c ? nv : nv0;
-        const uint32_t bytes = static_cast<uint32_t>(ve - vb) * 16u;
+        const uint32_t bytes = static_cast<uint32_t>((e1 - e0) * ESZ);
         if (!act || bytes == 0) {
-            mbar_arrive(bar_addr(c));
+            mbar_arrive(bar_addr(b));
             return;
         }
-        mbar_arrive_expect_tx(bar_addr(c), bytes * (KL ? 2u : 1u));
-        const size_t off = static_cast<size_t>(rr * p.ld + e0) * ESZ + static_cast<size_t>(vb) * 16;
-        bulk_load(buf_addr(0) + vb * 16, static_cast<const unsigned char*>(p.logits) + off, bytes, bar_addr(c));
+        mbar_arrive_expect_tx(bar_addr(b), bytes * (KL ? 2u : 1u));
+        const size_t off = static_cast<size_t>(rr * p.ld + e0) * ESZ;
+        bulk_load(buf_addr(b, 0), static_cast<const unsigned char*>(p.logits) + off, bytes, bar_addr(b));
         if (KL)
-            bulk_load(buf_addr(1) + vb * 16, static_cast<const unsigned char*>(p.teacher) + off, bytes, bar_addr(c));
+            bulk_load(buf_addr(b, 1), static_cast<const unsigned char*>(p.teacher) + off, bytes, bar_addr(b));
     };
 
-    if (tid == 0 && rowq[0] < p.T) issue(rowq[0], tq[0], 0);
+    if (tid == 0)
+        for (int k = 0; k < nbuf - 1; ++k)
+            if (rowq[k] < p.T) issue(rowq[k], tq[k], k);
 
     bool failed = false;
     for (int i = 0;; ++i) {
@@ -594,10 +580,12 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         __syncthreads();   // buffers, scratch and coefficients of the previous row are free
         int claim_row = 0;
         if (tid == 0) {
-            issue(r, tq[i & 3], 1);   // piece 1 of this row (piece 0 was issued a pass earlier)
-            if (rank == 0) claim_row = G + atomicAdd(p.ws.row_counter, 1);
+            const int j = (i + nbuf - 1) & 3;
+            if (rowq[j] < p.T) issue(rowq[j], tq[j], (i + nbuf - 1) % nbuf);
+            if (rank == 0) claim_row = nbuf * G + atomicAdd(p.ws.row_counter, 1);
         }
-        const uint32_t parity = static_cast<uint32_t>(i & 1);
+        const int b = i % nbuf;
+        const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
 
         const int64_t t = tq[i & 3];
         const bool act = t != -100;
@@ -605,17 +593,16 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         int64_t e0, e1;
         row_interior<ESZ>(p.logits, r, p.ld, c0, c1, e0, e1);
         const int nvec = static_cast<int>((e1 - e0) / VN);
-        const int nv0 = split(nvec);
         const size_t row_off = static_cast<size_t>(r * p.ld) * ESZ;
-        const uint32_t bz = buf_addr(0);
-        const uint32_t bu = KL ? buf_addr(1) : 0u;
+        const uint32_t bz = buf_addr(b, 0);
+        const uint32_t bu = KL ? buf_addr(b, 1) : 0u;
         const int64_t tv = t - e0;   // target offset within the interior (may be outside)
         const bool owner = act && t >= c0 && t < c1;
         // the one interior vector holding the target (-1 if none) and its lane
         const int vt = (act && tv >= 0 && tv < static_cast<int64_t>(nvec) * VN) ? static_cast<int>(tv / VN) : -1;
         const int kt = (vt >= 0) ? static_cast<int>(tv - static_cast<int64_t>(vt) * VN) : -1;
 
-        if (!failed && !mbar_wait_bounded(bar_addr(0), parity, kWaitLimitCycles)) {
+        if (!failed && !mbar_wait_bounded(bar_addr(b), parity, kWaitLimitCycles)) {
             set_error(p.ws.err, kErrTimeout);
             failed = true;
         }
@@ -639,41 +626,30 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             g_cr = (gs >= 0 && gs < p.num_segments) ? p.ws.seg_coef[gs] : 0.f;
         }
 
-        // ---- pass A: maxima (non-target for z, all columns for u), piece 0 while
-        // piece 1 may still be arriving
-        const bool pass_a = act && mode != kModeGrad;
-        uint32_t accz = IO::max_init(), accu = IO::max_init(), accn = IO::min_init();
-        float mx = -INFINITY, mu = -INFINITY, un = INFINITY;
-        auto max_vec = [&](int v) {
-            const uint4 q = lds128(bz + v * 16);
-            if (v == vt) {
-                float x[VN];
-                IO::unpack(q, x);
+        // ---- pass A: maxima (non-target for z, all columns for u)
+        if (act && mode != kModeGrad) {
+            uint32_t accz = IO::max_init(), accu = IO::max_init(), accn = IO::min_init();
+            float mx = -INFINITY, mu = -INFINITY, un = INFINITY;
+#pragma unroll 4
+            for (int v = tid; v < nvec; v += NT) {
+                const uint4 q = lds128(bz + v * 16);
+                if (v == vt) {
+                    float x[VN];
+                    IO::unpack(q, x);
 #pragma unroll
-                for (int j = 0; j < VN; ++j) {
-                    if (j != kt) mx = fmaxf(mx, x[j]);
-                    else slot[0] = x[j];
+                    for (int j = 0; j < VN; ++j) {
+                        if (j != kt) mx = fmaxf(mx, x[j]);
+                        else slot[0] = x[j];
+                    }
+                } else {
+                    accz = IO::max_acc(accz, q);
                 }
-            } else {
-                accz = IO::max_acc(accz, q);
+                if (KL) {
+                    const uint4 qu = lds128(bu + v * 16);
+                    accu = IO::max_acc(accu, qu);
+                    accn = IO::min_acc(accn, qu);
+                }
             }
-            if (KL) {
-                const uint4 qu = lds128(bu + v * 16);
-                accu = IO::max_acc(accu, qu);
-                accn = IO::min_acc(accn, qu);
-            }
-        };
-        if (pass_a) {
-#pragma unroll 4
-            for (int v = tid; v < nv0; v += NT) max_vec(v);
-        }
-        if (!failed && !mbar_wait_bounded(bar_addr(1), parity, kWaitLimitCycles)) {
-            set_error(p.ws.err, kErrTimeout);
-            failed = true;
-        }
-        if (pass_a) {
-#pragma unroll 4
-            for (int v = nv0 + tid; v < nvec; v += NT) max_vec(v);
             if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
@@ -1009,28 +985,18 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 if (p.kl_out) p.kl_out[r] = 0.f;
             }
             if (lane == 0) {
-                rowq[(i + 1) & 3] = next_row;
-                tq[(i + 1) & 3] = next_t;
+                rowq[(i + nbuf) & 3] = next_row;
+                tq[(i + nbuf) & 3] = next_t;
             }
         }
         __syncthreads();
 
-        // ---- pass C: gradient of the slice, written once, piece by piece; once
-        // every thread is done with piece 0, it takes piece 0 of the next row
-        for (int c = 0; c < 2; ++c) {
-            const int vb = c ? nv0 : 0, ve = c ? nvec : nv0;
-            if (c == 1) {
-                __syncthreads();
-                if (tid == 0) {
-                    const int j = (i + 1) & 3;
-                    if (rowq[j] < p.T) issue(rowq[j], tq[j], 0);
-                }
-            }
-            if (!p.grad || mode == kModeStats) continue;
+        // ---- pass C: gradient of the slice, written once
+        if (p.grad && mode != kModeStats) {
             unsigned char* g = static_cast<unsigned char*>(p.grad) + row_off + static_cast<size_t>(e0) * ESZ;
             if (!act) {
-                for (int v = vb + tid; v < ve; v += NT) stg128(g + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
-                if (c == 1 && tid == NT - 1) {
+                for (int v = tid; v < nvec; v += NT) stg128(g + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
+                if (tid == NT - 1) {
                     for (int64_t j = c0; j < e0; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
                     for (int64_t j = e1; j < c1; ++j) IO::store1(p.grad, r * p.ld + j, 0.f);
                 }
@@ -1044,7 +1010,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
                 const uint64_t neg1 = f2_pack(-1.f, -1.f);
 #pragma unroll 2
-                for (int v = vb + tid; v < ve; v += NT) {
+                for (int v = tid; v < nvec; v += NT) {
                     const uint4 q = lds128(bz + v * 16);
                     const uint4 qu = lds128(bu + v * 16);
                     float gv[VN];
@@ -1070,7 +1036,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 }
             } else if (KL) {
 #pragma unroll 2
-                for (int v = vb + tid; v < ve; v += NT) {
+                for (int v = tid; v < nvec; v += NT) {
                     float x[VN], y[VN], gv[VN], qv[VN];
                     IO::unpack(lds128(bz + v * 16), x);
                     IO::unpack(lds128(bu + v * 16), y);
@@ -1092,7 +1058,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
                     const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
 #pragma unroll 2
-                    for (int v = vb + tid; v < ve; v += NT) {
+                    for (int v = tid; v < nvec; v += NT) {
                         const uint4 q = lds128(bz + v * 16);
                         float gv[VN];
 #pragma unroll
@@ -1117,7 +1083,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 if (cf.neg) body(BoolConst<true>{});
                 else body(BoolConst<false>{});
             }
-            if (c == 1 && tid == NT - 1) {
+            if (tid == NT - 1) {
                 for (int pass = 0; pass < 2; ++pass) {
                     const int64_t lo = pass == 0 ? c0 : e1, hi = pass == 0 ? e0 : c1;
                     for (int64_t j = lo; j < hi; ++j) {

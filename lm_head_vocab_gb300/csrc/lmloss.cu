@@ -20,7 +20,7 @@ struct lmloss_ctx {
     int32_t max_S = 0;
     void* ws_mem = nullptr;
     Workspace ws{};
-    int cfg_cluster = 0, cfg_threads = 0, cfg_chunks = 0;
+    int cfg_cluster = 0, cfg_threads = 0, cfg_nbuf = 0;
     int timing = 0;
     static constexpr int kMaxTimed = 4096;
     cudaEvent_t* ev = nullptr;   // [2 * kMaxTimed], created on first use
@@ -114,13 +114,13 @@ const void* pick_fused(bool bf16, bool kl, int nt)
 
 struct FusedPlan {
     const void* fn = nullptr;
-    int C = 0, NT = 0, chunks = 0, grid = 0;
+    int C = 0, NT = 0, nbuf = 0, grid = 0;
     int64_t slice = 0;
     uint32_t buf_bytes = 0;
     size_t smem = 0;
 };
 
-size_t fused_smem(int64_t V, int C, bool kl, int esz, int64_t* slice_out, uint32_t* buf_out)
+size_t fused_smem(int64_t V, int C, int nbuf, bool kl, int esz, int64_t* slice_out, uint32_t* buf_out)
 {
     const int vn = 16 / esz;
     int64_t slice = (V + C - 1) / C;
@@ -128,7 +128,7 @@ size_t fused_smem(int64_t V, int C, bool kl, int esz, int64_t* slice_out, uint32
     const uint32_t buf = static_cast<uint32_t>(align_up(static_cast<size_t>(slice) * esz, 128));
     if (slice_out) *slice_out = slice;
     if (buf_out) *buf_out = buf;
-    return kHdrBytes + static_cast<size_t>(kl ? 2 : 1) * buf;
+    return kHdrBytes + static_cast<size_t>(nbuf) * (kl ? 2 : 1) * buf;
 }
 
 lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
@@ -140,7 +140,7 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
     // smallest cluster whose slice (logits, plus teacher) fits in 56 KB (112 KB
     // with a teacher), so that three (two) CTAs share an SM; and about 110
     // elements per thread, rounded to 128, 256 or 512 threads.
-    int chunks = h->cfg_chunks ? h->cfg_chunks : kDefaultChunks;
+    int nbuf = h->cfg_nbuf ? h->cfg_nbuf : 1;
     int C = h->cfg_cluster;
     if (!C) {
         const int64_t row_bytes = a->V * esz * (kl ? 2 : 1);
@@ -154,13 +154,13 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
         NT = per_thread < 181.0 ? 128 : (per_thread < 362.0 ? 256 : 512);
     }
     if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel
-    if (C < 1 || C > 16 || (chunks != 1 && chunks != 2)) return LMLOSS_ERR_UNSUPPORTED;
+    if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
     P.fn = pick_fused(bf16, kl, NT);
     if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
     P.C = C;
     P.NT = NT;
-    P.chunks = chunks;
-    P.smem = fused_smem(a->V, C, kl, esz, &P.slice, &P.buf_bytes);
+    P.nbuf = nbuf;
+    P.smem = fused_smem(a->V, C, nbuf, kl, esz, &P.slice, &P.buf_bytes);
     if (P.smem > static_cast<size_t>(h->smem_optin)) return LMLOSS_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(P.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P.smem)) != cudaSuccess)
         return LMLOSS_ERR_CUDA;
@@ -204,7 +204,7 @@ lmloss_status launch_fused(lmloss_ctx* h, const lmloss_args* a, CallParams& p, i
     p.mode = mode;
     p.cluster = P.C;
     p.slice = P.slice;
-    p.chunks = P.chunks;
+    p.nbuf = P.nbuf;
     p.buf_bytes = P.buf_bytes;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
@@ -226,7 +226,7 @@ lmloss_status launch_fused(lmloss_ctx* h, const lmloss_args* a, CallParams& p, i
     info.launches += 1;
     info.cluster = P.C;
     info.threads = P.NT;
-    info.chunks = P.chunks;
+    info.nbuf = P.nbuf;
     info.grid = P.grid;
     info.smem_bytes = static_cast<int32_t>(P.smem);
     return LMLOSS_OK;
@@ -325,16 +325,16 @@ lmloss_status lmloss_destroy(lmloss_handle h)
     return e == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
 }
 
-lmloss_status lmloss_set_launch_config(lmloss_handle h, int cluster, int threads, int chunks)
+lmloss_status lmloss_set_launch_config(lmloss_handle h, int cluster, int threads, int nbuf)
 {
     if (!h) return LMLOSS_ERR_INVALID_ARG;
     if (cluster < 0 || cluster > 16) return LMLOSS_ERR_INVALID_ARG;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512 && threads != 1024)
         return LMLOSS_ERR_INVALID_ARG;
-    if (chunks < 0 || chunks > 2) return LMLOSS_ERR_INVALID_ARG;
+    if (nbuf < 0 || nbuf > 2) return LMLOSS_ERR_INVALID_ARG;
     h->cfg_cluster = cluster;
     h->cfg_threads = threads;
-    h->cfg_chunks = chunks;
+    h->cfg_nbuf = nbuf;
     return LMLOSS_OK;
 }
 

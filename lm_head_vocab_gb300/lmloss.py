@@ -74,8 +74,8 @@ class LMLoss:
             pass
 
     # ------------------------------------------------------------- tuning
-    def set_launch_config(self, cluster: int = 0, threads: int = 0, chunks: int = 0):
-        st = _lib.lmloss_set_launch_config(self.handle, cluster, threads, chunks)
+    def set_launch_config(self, cluster: int = 0, threads: int = 0, nbuf: int = 0):
+        st = _lib.lmloss_set_launch_config(self.handle, cluster, threads, nbuf)
         if st != _lib.LMLOSS_OK:
             raise LMLossError(st, "lmloss_set_launch_config")
 

@@ -157,17 +157,17 @@ def test_deterministic_repeat(dev, handle):
     assert torch.equal(a.loss, b.loss)
 
 
-@pytest.mark.parametrize("cluster,threads,chunks", [(1, 256, 1), (2, 512, 2), (3, 512, 1), (4, 256, 2),
+@pytest.mark.parametrize("cluster,threads,nbuf", [(1, 256, 1), (2, 512, 2), (3, 512, 1), (4, 256, 2),
                                                   (8, 512, 2), (16, 128, 1)])
-def test_launch_shapes(dev, handle, cluster, threads, chunks):
+def test_launch_shapes(dev, handle, cluster, threads, nbuf):
     case = _case(dev, "ce_z_bf16", dict(T=96, V=50021))
     R, g_ref = oracle.forward_backward(case.P)
-    handle.set_launch_config(cluster, threads, chunks)
+    handle.set_launch_config(cluster, threads, nbuf)
     try:
         _, out = run(handle, case)
         info = handle.call_info()
-        assert info["cluster"] == cluster and info["threads"] == threads and info["chunks"] == chunks
-        compare_all(case, out, R, g_ref, f"shape {cluster},{threads},{chunks}")
+        assert info["cluster"] == cluster and info["threads"] == threads and info["nbuf"] == nbuf
+        compare_all(case, out, R, g_ref, f"shape {cluster},{threads},{nbuf}")
     finally:
         handle.set_launch_config(0, 0, 0)
 

@@ -350,7 +350,7 @@ struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
     float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
     float zt;           // target logit (on the CTA that owns the target column)
-    int next_row;       // rank 0: row for iteration i + nbuf
+    int next_row;       // rank 0: row for iteration i + depth (see fused_kernel)
     int next_t;         // rank 0: its target, or -100 when the row is inactive
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
     float pad0, pad1, pad2;
@@ -497,7 +497,10 @@ __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int
 template <bool KL, int NT>
 constexpr int fused_min_blocks() { return NT >= 1024 ? 1 : (KL ? 2 : 1024 / NT); }
 
-template <bool BF16, bool KL, int NT>
+// EARLY: the statistics pass (no gradient), which hands its buffer to the next
+// copy as soon as pass B is done; a separate instantiation, so that the passes
+// that write the gradient compile exactly as without it.
+template <bool BF16, bool KL, int NT, bool EARLY>
 __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel(const CallParams p)
 {
     using IO = Vec<BF16>;
@@ -526,6 +529,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     const int64_t c0 = min(p.V, static_cast<int64_t>(rank) * p.slice);
     const int64_t c1 = min(p.V, c0 + p.slice);
     const int nbuf = p.nbuf;
+    // Rows known ahead of the one in hand.  A pass that writes the gradient
+    // frees a buffer at the end of the row (the copy of row i + nbuf - 1 goes
+    // out at the top of row i); the statistics pass frees it after pass B, so
+    // the copy of row i + nbuf goes out then, under the record exchange, and
+    // the row after it must already be known.
+    constexpr bool early = EARLY;   // launched only with mode == kModeStats
+    const int depth = nbuf + (early ? 1 : 0);
     const float s_tok = token_scale(p);
     // Kernel-wide constants of the row coefficients: b = s w_kl and, when no
     // per-row term enters it (no z-loss, no policy term), a = s (w_ce + w_kl).
@@ -545,8 +555,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         mbar_init(smem_addr(&rbar[0]), 1);
         mbar_init(smem_addr(&rbar[1]), 1);
         for (int k = 0; k < 4; ++k) {
-            rowq[k] = (k < nbuf) ? cid + k * G : 0x7fffffff;
-            tq[k] = (k < nbuf && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
+            rowq[k] = (k < depth) ? cid + k * G : 0x7fffffff;
+            tq[k] = (k < depth && rowq[k] < p.T) ? row_target(p, rowq[k]) : -100;
         }
         fence_mbar_init();
     }
@@ -570,7 +580,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     };
 
     if (tid == 0)
-        for (int k = 0; k < nbuf - 1; ++k)
+        for (int k = 0; k < (early ? nbuf : nbuf - 1); ++k)
             if (rowq[k] < p.T) issue(rowq[k], tq[k], k);
 
     bool failed = false;
@@ -581,8 +591,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         int claim_row = 0;
         if (tid == 0) {
             const int j = (i + nbuf - 1) & 3;
-            if (rowq[j] < p.T) issue(rowq[j], tq[j], (i + nbuf - 1) % nbuf);
-            if (rank == 0) claim_row = nbuf * G + atomicAdd(p.ws.row_counter, 1);
+            if (!early && rowq[j] < p.T) issue(rowq[j], tq[j], (i + nbuf - 1) % nbuf);
+            if (rank == 0) claim_row = depth * G + atomicAdd(p.ws.row_counter, 1);
         }
         const int b = i % nbuf;
         const uint32_t parity = static_cast<uint32_t>((i / nbuf) & 1);
@@ -781,6 +791,14 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
         }
         __syncthreads();
+
+        // statistics pass: every thread is done with this buffer (passes A and B,
+        // after its wait), so it takes the copy of row i + nbuf now; the last
+        // warp issues it, leaving warp 0 free to publish the record
+        if (early && tid == NT - 32) {
+            const int j = (i + nbuf) & 3;
+            if (rowq[j] < p.T) issue(rowq[j], tq[j], b);
+        }
 
         // ---- publish this CTA's record
         if (warp == 0) {
@@ -985,8 +1003,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 if (p.kl_out) p.kl_out[r] = 0.f;
             }
             if (lane == 0) {
-                rowq[(i + nbuf) & 3] = next_row;
-                tq[(i + nbuf) & 3] = next_t;
+                rowq[(i + depth) & 3] = next_row;
+                tq[(i + depth) & 3] = next_t;
             }
         }
         __syncthreads();

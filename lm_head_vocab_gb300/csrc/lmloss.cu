@@ -95,14 +95,18 @@ lmloss_status check(const lmloss_args* a)
 
 // ------------------------------------------------------------ launch plans
 template <bool BF16, bool KL, int NT>
-const void* fused_ptr() { return reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT>); }
-
-const void* pick_fused(bool bf16, bool kl, int nt)
+const void* fused_ptr(bool stats)
 {
-#define LMLOSS_PICK(NTV)                                                            \
-    if (nt == NTV) {                                                                \
-        if (bf16) return kl ? fused_ptr<true, true, NTV>() : fused_ptr<true, false, NTV>(); \
-        return kl ? fused_ptr<false, true, NTV>() : fused_ptr<false, false, NTV>();  \
+    return stats ? reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT, true>)
+                 : reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT, false>);
+}
+
+const void* pick_fused(bool bf16, bool kl, int nt, bool stats)
+{
+#define LMLOSS_PICK(NTV)                                                                          \
+    if (nt == NTV) {                                                                              \
+        if (bf16) return kl ? fused_ptr<true, true, NTV>(stats) : fused_ptr<true, false, NTV>(stats); \
+        return kl ? fused_ptr<false, true, NTV>(stats) : fused_ptr<false, false, NTV>(stats);      \
     }
     LMLOSS_PICK(128)
     LMLOSS_PICK(256)
@@ -131,7 +135,7 @@ size_t fused_smem(int64_t V, int C, int nbuf, bool kl, int esz, int64_t* slice_o
     return kHdrBytes + static_cast<size_t>(nbuf) * (kl ? 2 : 1) * buf;
 }
 
-lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
+lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPlan& P)
 {
     const bool bf16 = a->dtype == LMLOSS_BF16;
     const bool kl = a->teacher_logits != nullptr;
@@ -155,7 +159,7 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, FusedPlan& P)
     }
     if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel
     if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
-    P.fn = pick_fused(bf16, kl, NT);
+    P.fn = pick_fused(bf16, kl, NT, mode == kModeStats);
     if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
     P.C = C;
     P.NT = NT;
@@ -199,7 +203,7 @@ lmloss_status launch_fused(lmloss_ctx* h, const lmloss_args* a, CallParams& p, i
                            lmloss_call_info& info)
 {
     FusedPlan P;
-    lmloss_status st = plan_fused(h, a, P);
+    lmloss_status st = plan_fused(h, a, mode, P);
     if (st != LMLOSS_OK) return st;
     p.mode = mode;
     p.cluster = P.C;

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 constexpr int kHdrBytes = 3072;   // mbarriers, row queue, cluster records, warp scratch
 constexpr int kMaxCluster = 16;
 
-struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
+struct ClusterRec {     // one CTA's partial for the current row (32 bytes, 48 with the entropy)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
     float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
     float zt;           // target logit (on the CTA that owns the target column)
@@ -355,7 +355,7 @@ struct ClusterRec {     // one CTA's partial for the current row (48 bytes)
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
     float pad0, pad1, pad2;
 };
-static_assert(sizeof(ClusterRec) == 48, "record is three 16-byte pushes");
+static_assert(sizeof(ClusterRec) == 48, "record is two or three 16-byte pushes");
 
 struct RowCoef {        // the row's gradient coefficients, shared by the CTA's threads
     float cz;           // a p_j = sign(a) 2^(z_j log2e - cz)
@@ -847,13 +847,16 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const uint4* Rv = reinterpret_cast<const uint4*>(&R);
             const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
             const uint32_t my_bar = smem_addr(&rbar[i & 1]);
-            if (lane == 0) mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C * sizeof(ClusterRec)));
+            // the entropy partial travels only when the entropy is wanted
+            const bool ent = p.entropy_out != nullptr;
+            const uint32_t rec_bytes = ent ? 48u : 32u;
+            if (lane == 0) mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C) * rec_bytes);
             if (lane < C) {
                 const uint32_t dst = dsmem_map(my_slot, static_cast<uint32_t>(lane));
                 const uint32_t bar = dsmem_map(my_bar, static_cast<uint32_t>(lane));
                 st_async_v4(dst, Rv[0], bar);
                 st_async_v4(dst + 16, Rv[1], bar);
-                st_async_v4(dst + 32, Rv[2], bar);
+                if (ent) st_async_v4(dst + 32, Rv[2], bar);
             }
         }
 
@@ -900,7 +903,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const float fz = rescale(q.m, M);
                 float S = q.s * fz;
                 // sum e^(z - M) (z - M) over this CTA's non-target columns
-                float Bc = (q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
+                const bool ent = p.entropy_out != nullptr;
+                float Bc = (!ent || q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
                 float Zt = q.zt;   // summed below: every record but the owner's holds exactly 0
                 float Mu = q.mu, Su = 0.f, W = 0.f;
                 if (KL) {
@@ -913,7 +917,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     S += __shfl_xor_sync(0xffffffffu, S, off);
-                    Bc += __shfl_xor_sync(0xffffffffu, Bc, off);
+                    if (ent) Bc += __shfl_xor_sync(0xffffffffu, Bc, off);
                     Zt += __shfl_xor_sync(0xffffffffu, Zt, off);
                     if (KL) {
                         Su += __shfl_xor_sync(0xffffffffu, Su, off);

@@ -636,7 +636,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             g_cr = (gs >= 0 && gs < p.num_segments) ? p.ws.seg_coef[gs] : 0.f;
         }
 
-        // ---- pass A: maxima (non-target for z, all columns for u)
+        // ---- pass A: maxima (non-target for z, all columns for u), per warp: each
+        // warp takes its sums against its own maxima and the warps' partials are
+        // rebased once, when the CTA's record is built, so no CTA barrier sits
+        // between the two passes
+        float m_w = -INFINITY, mu_w = -INFINITY, un_w = INFINITY;
         if (act && mode != kModeGrad) {
             uint32_t accz = IO::max_init(), accu = IO::max_init(), accn = IO::min_init();
             float mx = -INFINITY, mu = -INFINITY, un = INFINITY;
@@ -687,38 +691,23 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     un = fminf(un, __shfl_xor_sync(0xffffffffu, un, off));
                 }
             }
-            if (lane == 0) {
-                wred[warp] = m;
-                if (KL) { wred[32 + warp] = mu; wred[160 + warp] = un; }
-            }
+            m_w = m;
+            if (KL) { mu_w = mu; un_w = un; }
         }
-        __syncthreads();
 
-        // ---- pass B: sums relative to the CTA maximum
-        float m_cta = -INFINITY, mu_cta = -INFINITY;
+        // ---- pass B: sums relative to the warp's maxima
         if (act && mode != kModeGrad) {
-            m_cta = (lane < NW) ? wred[lane] : -INFINITY;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
-            if (KL) {
-                mu_cta = (lane < NW) ? wred[32 + lane] : -INFINITY;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
-            }
-            const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
-            const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
+            const float mL = (m_w == -INFINITY) ? 0.f : m_w * kLog2e;
+            const float muL = (mu_w == -INFINITY) ? 0.f : mu_w * kLog2e;
             float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f;
             if (!KL) {
                 if (p.entropy_out) sums_plain<IO, NT, true>(bz, nvec, tid, vt, kt, mL, s0, b0);
                 else sums_plain<IO, NT, false>(bz, nvec, tid, vt, kt, mL, s0, b0);
             }
             if (KL) {
-                // with no -inf teacher logit in the slice, e^(u-mu) (u - z) needs no guard
-                float un_cta = (lane < NW) ? wred[160 + lane] : INFINITY;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) un_cta = fminf(un_cta, __shfl_xor_sync(0xffffffffu, un_cta, off));
-                if (un_cta > -INFINITY) {
+                // with no -inf teacher logit in the warp's columns, e^(u-mu) (u - z)
+                // needs no guard
+                if (un_w > -INFINITY) {
                     if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
                     else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
                 } else {
@@ -785,9 +774,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 }
             }
             if (lane == 0) {
+                wred[warp] = m_w;
                 wred[64 + warp] = s;
                 wred[192 + warp] = b0;
-                if (KL) { wred[96 + warp] = su; wred[128 + warp] = w; }
+                if (KL) { wred[32 + warp] = mu_w; wred[96 + warp] = su; wred[128 + warp] = w; }
             }
         }
         __syncthreads();
@@ -803,12 +793,35 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         // ---- publish this CTA's record
         if (warp == 0) {
             float s = 0.f, su = 0.f, w = 0.f, bc = 0.f;
+            float m_cta = -INFINITY, mu_cta = -INFINITY;
             if (act) {
+                // warp w's sums are against round(m_w log2e): rebase them onto
+                // round(m_cta log2e) (entropy partial: e (a + d) summed = f (b + s d))
+                const float mw = (lane < NW) ? wred[lane] : -INFINITY;
+                m_cta = mw;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
+                const float mLc = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
+                const float mLw = (mw == -INFINITY) ? 0.f : mw * kLog2e;
                 s = (lane < NW) ? wred[64 + lane] : 0.f;
                 bc = (lane < NW) ? wred[192 + lane] : 0.f;
+                const float dz = mLw - mLc;
+                const float fz = (s == 0.f) ? 0.f : ex2(dz);
+                bc = (s == 0.f) ? 0.f : fz * fmaf(s, dz, bc);
+                s *= fz;
                 if (KL) {
+                    const float muw = (lane < NW) ? wred[32 + lane] : -INFINITY;
+                    mu_cta = muw;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
+                    const float muLc = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
+                    const float muLw = (muw == -INFINITY) ? 0.f : muw * kLog2e;
                     su = (lane < NW) ? wred[96 + lane] : 0.f;
                     w = (lane < NW) ? wred[128 + lane] : 0.f;
+                    const float fu = (su == 0.f) ? 0.f : ex2(muLw - muLc);
+                    su *= fu;
+                    w *= fu;
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {

@@ -434,8 +434,9 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
     const uint64_t nmu2 = f2_pack(-muL, -muL);
     const uint64_t neg1 = f2_pack(-1.f, -1.f);
     uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz, accb = accz;
-#pragma unroll 2
-    for (int v = tid; v < nvec; v += NT) {
+    // one vector: the student terms of every column but lane `kill` (the
+    // target's, or -1), the teacher terms of every column
+    auto vec = [&](int v, int kill) {
         const uint4 q = lds128(bz + v * 16);
         const uint4 qu = lds128(bu + v * 16);
 #pragma unroll
@@ -446,10 +447,8 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
             f2_unpack(argz, a0, a1);
             f2_unpack(f2_fma(xu, L2, nmu2), u0, u1);
             float e0 = ex2(a0), e1 = ex2(a1);
-            if (v == vt) {
-                if (2 * k == kt) e0 = 0.f;
-                if (2 * k + 1 == kt) e1 = 0.f;
-            }
+            if (2 * k == kill) e0 = 0.f;
+            if (2 * k + 1 == kill) e1 = 0.f;
             const uint64_t ez = f2_pack(e0, e1);
             accz = f2_add(accz, ez);
             if (ENT) accb = f2_fma(ez, argz, accb);
@@ -457,7 +456,13 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
             accu = f2_add(accu, eu);
             accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
         }
-    }
+    };
+    // the target's vector is taken out of the loop, so the loop body needs no
+    // per-column test
+#pragma unroll 2
+    for (int v = tid; v < nvec; v += NT)
+        if (v != vt) vec(v, -1);
+    if (vt >= 0 && vt % NT == tid) vec(vt, kt);
     float h0, h1;
     f2_unpack(accz, h0, h1);
     s_out = h0 + h1;
@@ -1044,8 +1049,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
                 const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
                 const uint64_t neg1 = f2_pack(-1.f, -1.f);
-#pragma unroll 2
-                for (int v = tid; v < nvec; v += NT) {
+                auto vec = [&](int v, int tcol) {
                     const uint4 q = lds128(bz + v * 16);
                     const uint4 qu = lds128(bu + v * 16);
                     float gv[VN];
@@ -1058,17 +1062,22 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         const uint64_t ap = f2_pack(ex2(a0), ex2(a1));
                         float g0, g1;
                         f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
-                        if (v == vt) {
+                        if (tcol >= 0) {
                             float q0, q1;
                             f2_unpack(bq, q0, q1);
-                            if (2 * k == kt) g0 = cf.gt - q0;
-                            if (2 * k + 1 == kt) g1 = cf.gt - q1;
+                            if (2 * k == tcol) g0 = cf.gt - q0;
+                            if (2 * k + 1 == tcol) g1 = cf.gt - q1;
                         }
                         gv[2 * k] = g0;
                         gv[2 * k + 1] = g1;
                     }
                     stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
-                }
+                };
+                // the target's vector out of the loop: no per-column test inside it
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT)
+                    if (v != vt) vec(v, -1);
+                if (vt >= 0 && vt % NT == tid) vec(vt, kt);
             } else if (KL) {
 #pragma unroll 2
                 for (int v = tid; v < nvec; v += NT) {

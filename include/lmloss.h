@@ -222,6 +222,39 @@ lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info)
 #define LMLOSS_NOALLOC_MAX_SEGMENTS 4096
 lmloss_status lmloss_forward_backward_noalloc(const lmloss_args* args, cudaStream_t stream);
 
+/* ---- Vocabulary-split rows (the vocabulary of each row spread over K shards)
+ *
+ * torchtitan PR 5661, "Numerics (TP > 1 only)": with the vocabulary split over
+ * devices, each shard drops the target from its own sum of exponentials and
+ * only per-row statistics are combined.  Here the K shards are K separate
+ * [T, V_k] logit matrices on one GPU, holding the columns [v0_k, v0_k + V_k)
+ * of a V_total-wide vocabulary.  Three steps, in order, on one handle, with no
+ * other call on that handle in between (the merge leaves the rows' statistics
+ * in its workspace for the gradient step); cross-entropy and z-loss only (a
+ * teacher, GSPO, GRPO, the entropy or per-row KL: LMLOSS_ERR_UNSUPPORTED).
+ *
+ * lmloss_shard_stats: for each active row, the shard's maximum over its
+ *   non-target columns, the sum of e^(z - max) over them, the target logit if
+ *   the shard holds the target column and 1.0 / 0.0 for "holds it", into
+ *   part_out[4 T] (device, fp32, caller-owned).  `args` describes the shard:
+ *   logits [T, ld] with V = V_k columns, targets in global column numbers
+ *   [0, V_total).  grad_out and loss_out are ignored.
+ * lmloss_shard_merge: merges the K shards' partials (parts: host array of K
+ *   <= 16 device pointers) in shard order into each row's NLL and lse; writes
+ *   loss_out (CE and z-loss with the call's reduction; the KL and policy slots
+ *   are 0), logp_out / lse_out / count_out if given.  `args`: T, V = V_total,
+ *   targets, loss_mask, ce_weight, z_alpha, reduction, denominator; logits are
+ *   not read.  A row whose target no shard holds sets LMLOSS_ERR_BAD_TARGET.
+ * lmloss_shard_grad: writes the shard's gradient (grad_out, [T, ld], may alias
+ *   the shard's logits) from the merged statistics: the same bits as a
+ *   whole-row call would give each column, up to the order of the merge. */
+lmloss_status lmloss_shard_stats(lmloss_handle handle, const lmloss_args* args, int64_t v0, int64_t V_total,
+                                 float* part_out, cudaStream_t stream);
+lmloss_status lmloss_shard_merge(lmloss_handle handle, const lmloss_args* args, const float* const* parts,
+                                 int32_t K, cudaStream_t stream);
+lmloss_status lmloss_shard_grad(lmloss_handle handle, const lmloss_args* args, int64_t v0, int64_t V_total,
+                                cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -123,6 +123,11 @@ def load() -> ctypes.CDLL:
         "lmloss_get_timing": ([h, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)], st),
         "lmloss_get_call_info": ([h, ctypes.POINTER(lmloss_call_info)], st),
         "lmloss_selftest_bounded_wait": ([h, ctypes.c_longlong], st),
+        "lmloss_shard_stats": ([h, ctypes.POINTER(lmloss_args), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                ctypes.c_void_p], st),
+        "lmloss_shard_merge": ([h, ctypes.POINTER(lmloss_args), ctypes.POINTER(ctypes.c_void_p), ctypes.c_int32,
+                                ctypes.c_void_p], st),
+        "lmloss_shard_grad": ([h, ctypes.POINTER(lmloss_args), ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p], st),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -192,6 +192,9 @@ constexpr int kRedBlocks = 64;   // blocks of the count and reduce kernels
 // statistics alone (forward only, and the first pass of GSPO); the gradient
 // alone from statistics already in the workspace (GSPO's pass after its seam).
 enum : int { kModeFused = 0, kModeStats = 1, kModeGrad = 2 };
+// row_target of an active row whose target column lies in another vocabulary shard
+constexpr int kTargetElsewhere = -2;
+constexpr int kMaxShards = 16;
 
 struct CallParams {
     const void* logits;
@@ -219,6 +222,10 @@ struct CallParams {
     float* seg_loss_out;
     const float* tok_adv;   // GRPO per-token advantages, or null
     float* entropy_out;
+    // vocabulary shard: this call's columns are [col0, col0 + V) of v_total
+    // (col0 = 0, v_total = V for a whole row)
+    int64_t col0, v_total;
+    float* part_out;        // shard statistics pass: [T, 4] max, sum, target logit, owns target
     Workspace ws;
     // fused-kernel launch shape and mode
     int mode;               // kModeFused, kModeStats or kModeGrad
@@ -234,15 +241,35 @@ __device__ __forceinline__ bool row_active(const CallParams& p, int64_t r, int64
     return t != -100 && (p.mask == nullptr || p.mask[r] != 0);
 }
 
-// Target of row r as an int, -100 when the row takes no part; out-of-range
-// targets keep a value outside [0, V) (clamped into int range).
+// Target of row r as a column of this call's logits, -100 when the row takes
+// no part, kTargetElsewhere when it lies in another vocabulary shard;
+// out-of-range targets keep a value outside [0, V) (clamped into int range).
 __device__ __forceinline__ int row_target(const CallParams& p, int64_t r)
 {
     int64_t t;
     if (!row_active(p, r, t)) return -100;
     if (t < 0) return -1;
-    if (t >= p.V) return 0x7fffffff;
+    if (t >= p.v_total) return 0x7fffffff;
+    t -= p.col0;
+    if (t < 0 || t >= p.V) return kTargetElsewhere;
     return static_cast<int>(t);
+}
+
+// Cross-entropy scalars of a row from its non-target maximum M, the sum
+// S = sum_{j != t} e^(z_j - M) and the target logit, in fp32 with no step
+// that cancels:  lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S,
+// NLL = softplus(d),  lse = lse_nt + softplus(-d).
+__device__ __forceinline__ void ce_scalars(float M, float S, float zt, float& nll, float& lse, float& lnS,
+                                           float& sp_neg)
+{
+    lnS = (S == 0.f) ? -INFINITY : logf(S);
+    const float d = (M - zt) + lnS;
+    // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|): one exp, one log1p
+    const float l1p = log1pf(expf(-fabsf(d)));
+    nll = fmaxf(d, 0.f) + l1p;
+    sp_neg = fmaxf(-d, 0.f) + l1p;
+    lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
+    if (isnan(d)) lse = d;
 }
 
 // Token scale s: 1/N_active (token mean, 0 if none) or 1/denominator (SUM).
@@ -287,7 +314,7 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
         int64_t t;
         if (row_active(p, r, t)) {
             ++n;
-            if (t < 0 || t >= p.V) set_error(p.ws.err, kErrBadTarget);
+            if (t < 0 || t >= p.v_total) set_error(p.ws.err, kErrBadTarget);
         }
     }
     for (int i = blockIdx.x * blockDim.x + tid; i < p.num_segments; i += nb * blockDim.x) {
@@ -604,7 +631,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 
         const int64_t t = tq[i & 3];
         const bool act = t != -100;
-        const bool bad = act && (t < 0 || t >= p.V);
+        const bool elsewhere = t == kTargetElsewhere;   // target in another vocabulary shard
+        const bool bad = act && !elsewhere && (t < 0 || t >= p.V);
         int64_t e0, e1;
         row_interior<ESZ>(p.logits, r, p.ld, c0, c1, e0, e1);
         const int nvec = static_cast<int>((e1 - e0) / VN);
@@ -943,19 +971,23 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     }
                 }
                 const float ztf = Zt;
-                if (lane == 0) {
+                if (p.part_out) {
+                    // vocabulary shard, statistics pass: the shard's partials go out as they
+                    // are and are merged across shards by shard_merge_kernel
+                    if (lane == 0 && rank == 0) {
+                        float* o = p.part_out + 4 * r;
+                        o[0] = M;
+                        o[1] = S;
+                        o[2] = ztf;
+                        o[3] = (!bad && !elsewhere) ? 1.f : 0.f;
+                    }
+                } else if (lane == 0) {
                     // fp32 throughout, arranged so that no step cancels:
                     //   lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S  (M - z_t exact),
                     //   NLL = softplus(d),  lse = lse_nt + softplus(-d)
                     const float zt = bad ? __int_as_float(0x7fc00000) : ztf;
-                    const float lnS = (S == 0.f) ? -INFINITY : logf(S);
-                    const float d = (M - zt) + lnS;
-                    // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|): one exp, one log1p
-                    const float l1p = log1pf(expf(-fabsf(d)));
-                    const float nll = fmaxf(d, 0.f) + l1p;
-                    const float sp_neg = fmaxf(-d, 0.f) + l1p;   // softplus(-d)
-                    float lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
-                    if (isnan(d)) lse = d;
+                    float nll, lse, lnS, sp_neg;
+                    ce_scalars(M, S, zt, nll, lse, lnS, sp_neg);
                     const float pt = expf(-nll);
                     const float tg = (pt < 0.25f) ? pt - 1.0f : expm1f(-nll);
                     float kl = 0.f, dlu = 0.f;
@@ -1019,6 +1051,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 }
             } else if (lane == 0 && rank == 0 && mode != kModeGrad) {
                 p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f; p.ws.row_pol[r] = 0.f;
+                if (p.part_out) {
+                    float* o = p.part_out + 4 * r;
+                    o[0] = -INFINITY; o[1] = 0.f; o[2] = 0.f; o[3] = 0.f;
+                }
                 if (p.entropy_out) p.entropy_out[r] = 0.f;
                 if (p.logp_out) p.logp_out[r] = 0.f;
                 if (p.lse_out) p.lse_out[r] = 0.f;
@@ -1147,6 +1183,53 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         }
     }
     cluster_sync_all();   // no CTA leaves while a peer may still read its records
+}
+
+// ======================================================================
+// Vocabulary-split rows: the merge of the K shards' partials of each row
+// (max M_k, sum S_k against it, target logit where the shard holds it) into
+// the row's NLL and lse, as the record merge does across a cluster:
+// M = max M_k, S = sum_k S_k e^(M_k - M) in shard order, then ce_scalars.
+// torchtitan PR 5661, "Numerics (TP > 1 only)": each vocabulary shard drops
+// the target from its own sum; only the statistics are combined.
+// ======================================================================
+struct ShardParts {
+    const float* part[kMaxShards];   // [T, 4] each
+    int K;
+};
+
+__global__ void __launch_bounds__(256) shard_merge_kernel(const CallParams p, const ShardParts sp)
+{
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < p.T;
+         r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int64_t t;
+        float nll = 0.f, lse = 0.f;
+        if (row_active(p, r, t)) {
+            float M = -INFINITY;
+            for (int k = 0; k < sp.K; ++k) M = fmaxf(M, sp.part[k][4 * r]);
+            float S = 0.f, zt = 0.f;
+            int owners = 0;
+            for (int k = 0; k < sp.K; ++k) {
+                const float* q = sp.part[k] + 4 * r;
+                if (q[1] != 0.f) S += q[1] * rescale(q[0], M);
+                if (q[3] != 0.f) { zt = q[2]; ++owners; }
+            }
+            if (owners != 1 || t < 0 || t >= p.v_total) {
+                // target outside [0, V) (flagged by the count) or held by no shard
+                if (owners != 1) set_error(p.ws.err, kErrBadTarget);
+                nll = lse = __int_as_float(0x7fc00000);
+            } else {
+                float lnS, sp_neg;
+                ce_scalars(M, S, zt, nll, lse, lnS, sp_neg);
+            }
+        }
+        p.ws.row_nll[r] = nll;
+        p.ws.row_lse[r] = lse;
+        p.ws.row_kl[r] = 0.f;
+        p.ws.row_pol[r] = 0.f;
+        if (p.logp_out) p.logp_out[r] = -nll;
+        if (p.lse_out) p.lse_out[r] = lse;
+    }
 }
 
 // ======================================================================

@@ -54,13 +54,15 @@ bool misaligned(const void* a, const void* b)
     return ((reinterpret_cast<uintptr_t>(a) - reinterpret_cast<uintptr_t>(b)) & 15u) != 0;
 }
 
-lmloss_status check(const lmloss_args* a)
+// need_loss: the call writes loss_out (every call but the shard passes that
+// only read or write per-row data)
+lmloss_status check(const lmloss_args* a, bool need_loss = true)
 {
     if (!a) return LMLOSS_ERR_INVALID_ARG;
     if (a->T < 0 || a->V < 1 || a->ld < a->V) return LMLOSS_ERR_INVALID_ARG;
     if (a->dtype != LMLOSS_BF16 && a->dtype != LMLOSS_FP32) return LMLOSS_ERR_INVALID_ARG;
     if (a->reduction != LMLOSS_REDUCE_SUM && a->reduction != LMLOSS_REDUCE_TOKEN_MEAN) return LMLOSS_ERR_INVALID_ARG;
-    if (!a->loss_out) return LMLOSS_ERR_INVALID_ARG;
+    if (need_loss && !a->loss_out) return LMLOSS_ERR_INVALID_ARG;
     const int esz = a->dtype == LMLOSS_BF16 ? 2 : 4;
     if (a->T > 0) {
         if (!a->logits || !a->targets) return LMLOSS_ERR_INVALID_ARG;
@@ -191,6 +193,46 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     if (want < 1) want = 1;
     P.grid = static_cast<int>(want) * C;
     return LMLOSS_OK;
+}
+
+void fill_params(const lmloss_ctx* h, const lmloss_args* a, CallParams& p)
+{
+    const bool kl = a->teacher_logits != nullptr;
+    const bool gspo = a->segment_ids != nullptr;
+    p.logits = a->logits;
+    p.teacher = a->teacher_logits;
+    p.grad = a->grad_out;
+    p.targets = a->targets;
+    p.mask = a->loss_mask;
+    p.T = a->T;
+    p.V = a->V;
+    p.ld = a->ld;
+    p.w_ce = a->ce_weight;
+    p.alpha = a->z_alpha;
+    p.w_kl = kl ? a->kl_weight : 0.f;
+    p.reduction = a->reduction;
+    p.inv_denominator = a->reduction == LMLOSS_REDUCE_SUM ? 1.0 / a->denominator : 0.0;
+    p.seg_ids = a->segment_ids;
+    p.num_segments = gspo ? a->num_segments : 0;
+    p.adv = a->advantages;
+    p.old_logp = a->old_logprobs;
+    p.eps_lo = a->clip_eps_low;
+    p.eps_hi = a->clip_eps_high;
+    p.loss_out = a->loss_out;
+    p.logp_out = a->logp_out;
+    p.lse_out = a->lse_out;
+    p.kl_out = a->kl_out;
+    p.count_out = a->count_out;
+    p.seg_count_out = a->seg_count_out;
+    p.seg_ratio_out = a->seg_ratio_out;
+    p.seg_flag_out = a->seg_flag_out;
+    p.seg_loss_out = a->seg_loss_out;
+    p.tok_adv = a->token_advantages;
+    p.entropy_out = a->entropy_out;
+    p.ws = h->ws;
+    p.col0 = 0;
+    p.v_total = a->V;
+    p.part_out = nullptr;
 }
 
 lmloss_status launch_err()
@@ -409,41 +451,10 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     DeviceGuard g(h->device);
     if (!g.ok) return LMLOSS_ERR_CUDA;
 
-    const bool kl = a->teacher_logits != nullptr;
     const bool gspo = a->segment_ids != nullptr;
 
     CallParams p{};
-    p.logits = a->logits;
-    p.teacher = a->teacher_logits;
-    p.grad = a->grad_out;
-    p.targets = a->targets;
-    p.mask = a->loss_mask;
-    p.T = a->T;
-    p.V = a->V;
-    p.ld = a->ld;
-    p.w_ce = a->ce_weight;
-    p.alpha = a->z_alpha;
-    p.w_kl = kl ? a->kl_weight : 0.f;
-    p.reduction = a->reduction;
-    p.inv_denominator = a->reduction == LMLOSS_REDUCE_SUM ? 1.0 / a->denominator : 0.0;
-    p.seg_ids = a->segment_ids;
-    p.num_segments = gspo ? a->num_segments : 0;
-    p.adv = a->advantages;
-    p.old_logp = a->old_logprobs;
-    p.eps_lo = a->clip_eps_low;
-    p.eps_hi = a->clip_eps_high;
-    p.loss_out = a->loss_out;
-    p.logp_out = a->logp_out;
-    p.lse_out = a->lse_out;
-    p.kl_out = a->kl_out;
-    p.count_out = a->count_out;
-    p.seg_count_out = a->seg_count_out;
-    p.seg_ratio_out = a->seg_ratio_out;
-    p.seg_flag_out = a->seg_flag_out;
-    p.seg_loss_out = a->seg_loss_out;
-    p.tok_adv = a->token_advantages;
-    p.entropy_out = a->entropy_out;
-    p.ws = h->ws;
+    fill_params(h, a, p);
 
     lmloss_call_info info{};
 
@@ -496,6 +507,122 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     reduce_kernel<<<red_blocks, 256, 0, stream>>>(p);
     if ((st = launch_err()) != LMLOSS_OK) return st;
     info.launches += 1;
+    h->info = info;
+    return LMLOSS_OK;
+}
+
+// ------------------------------------------------- vocabulary-split rows
+// Arguments of a shard call: cross-entropy and z-loss only.
+static lmloss_status check_shard(const lmloss_args* a, int64_t v0, int64_t V_total)
+{
+    if (!a) return LMLOSS_ERR_INVALID_ARG;
+    if (a->teacher_logits || a->segment_ids || a->token_advantages || a->entropy_out || a->kl_out)
+        return LMLOSS_ERR_UNSUPPORTED;
+    if (v0 < 0 || V_total < 1 || a->V < 1 || v0 > V_total - a->V) return LMLOSS_ERR_INVALID_ARG;
+    if (V_total > (int64_t(1) << 31) - 8) return LMLOSS_ERR_UNSUPPORTED;   // targets as int in the kernel
+    return LMLOSS_OK;
+}
+
+static lmloss_status shard_prologue(lmloss_handle h, const lmloss_args* a, CallParams& p, int64_t v0, int64_t V_total,
+                             cudaStream_t stream)
+{
+    fill_params(h, a, p);
+    p.col0 = v0;
+    p.v_total = V_total;
+    int64_t rb = (a->T + 63) / 64;
+    if (rb > kRedBlocks) rb = kRedBlocks;
+    // the count gives the token scale, checks targets against the whole vocabulary
+    // and resets the row counter of the fused kernel
+    count_kernel<<<rb < 1 ? 1 : static_cast<unsigned>(rb), 256, 0, stream>>>(p);
+    return launch_err();
+}
+
+lmloss_status lmloss_shard_stats(lmloss_handle h, const lmloss_args* a, int64_t v0, int64_t V_total,
+                                 float* part_out, cudaStream_t stream)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    lmloss_status st = check_shard(a, v0, V_total);
+    if (st != LMLOSS_OK) return st;
+    lmloss_args b = *a;
+    b.grad_out = nullptr;
+    if ((st = check(&b, false)) != LMLOSS_OK) return st;
+    if (a->T > h->max_T || (a->T > 0 && !part_out)) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    CallParams p{};
+    if ((st = shard_prologue(h, &b, p, v0, V_total, stream)) != LMLOSS_OK) return st;
+    p.loss_out = nullptr;
+    p.logp_out = p.lse_out = nullptr;
+    p.part_out = part_out;
+    lmloss_call_info info{};
+    info.launches = 1;
+    if (a->T > 0 && (st = launch_fused(h, &b, p, kModeStats, stream, info)) != LMLOSS_OK) return st;
+    info.path = 3;
+    h->info = info;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_shard_merge(lmloss_handle h, const lmloss_args* a, const float* const* parts, int32_t K,
+                                 cudaStream_t stream)
+{
+    if (!h || !a) return LMLOSS_ERR_INVALID_ARG;
+    lmloss_status st = check_shard(a, 0, a->V);
+    if (st != LMLOSS_OK) return st;
+    if (K < 1 || K > kMaxShards || !parts) return LMLOSS_ERR_INVALID_ARG;
+    if (a->T < 0 || a->T > h->max_T || !a->loss_out) return LMLOSS_ERR_INVALID_ARG;
+    if (a->T > 0 && !a->targets) return LMLOSS_ERR_INVALID_ARG;
+    if (a->reduction != LMLOSS_REDUCE_SUM && a->reduction != LMLOSS_REDUCE_TOKEN_MEAN) return LMLOSS_ERR_INVALID_ARG;
+    if (a->reduction == LMLOSS_REDUCE_SUM && !(a->denominator > 0.0 && std::isfinite(a->denominator)))
+        return LMLOSS_ERR_INVALID_ARG;
+    if (!std::isfinite(a->ce_weight) || !std::isfinite(a->z_alpha)) return LMLOSS_ERR_INVALID_ARG;
+    ShardParts sp{};
+    sp.K = K;
+    for (int k = 0; k < K; ++k) {
+        if (a->T > 0 && !parts[k]) return LMLOSS_ERR_INVALID_ARG;
+        sp.part[k] = parts[k];
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    CallParams p{};
+    if ((st = shard_prologue(h, a, p, 0, a->V, stream)) != LMLOSS_OK) return st;
+    lmloss_call_info info{};
+    info.launches = 1;
+    if (a->T > 0) {
+        int64_t gb = (a->T + 255) / 256;
+        if (gb > 4LL * h->num_sms) gb = 4LL * h->num_sms;
+        shard_merge_kernel<<<static_cast<unsigned>(gb), 256, 0, stream>>>(p, sp);
+        if ((st = launch_err()) != LMLOSS_OK) return st;
+        info.launches += 1;
+    }
+    int64_t rb = (a->T + 63) / 64;
+    if (rb > kRedBlocks) rb = kRedBlocks;
+    reduce_kernel<<<rb < 1 ? 1 : static_cast<unsigned>(rb), 256, 0, stream>>>(p);
+    if ((st = launch_err()) != LMLOSS_OK) return st;
+    info.launches += 1;
+    info.path = 3;
+    h->info = info;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_shard_grad(lmloss_handle h, const lmloss_args* a, int64_t v0, int64_t V_total,
+                                cudaStream_t stream)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    lmloss_status st = check_shard(a, v0, V_total);
+    if (st != LMLOSS_OK) return st;
+    const lmloss_args b = *a;
+    if ((st = check(&b, false)) != LMLOSS_OK) return st;
+    if (a->T > h->max_T || (a->T > 0 && !a->grad_out)) return LMLOSS_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    CallParams p{};
+    if ((st = shard_prologue(h, &b, p, v0, V_total, stream)) != LMLOSS_OK) return st;
+    p.loss_out = nullptr;
+    p.logp_out = p.lse_out = nullptr;
+    lmloss_call_info info{};
+    info.launches = 1;
+    if (a->T > 0 && (st = launch_fused(h, &b, p, kModeGrad, stream, info)) != LMLOSS_OK) return st;
+    info.path = 3;
     h->info = info;
     return LMLOSS_OK;
 }

@@ -9,6 +9,8 @@ from __future__ import annotations
 from dataclasses import dataclass
 from typing import Optional, Union
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -200,6 +202,71 @@ class LMLoss:
         args, out, _keep = self.build_args(logits, targets, loss_mask, **kw)
         self.call(args, stream)
         return out
+
+    # ------------------------------------------- vocabulary-split rows
+    def _stream(self, stream):
+        return (torch.cuda.current_stream(self.device) if stream is None else stream).cuda_stream
+
+    def shard_stats(self, logits: torch.Tensor, targets: torch.Tensor, loss_mask=None, *, v0: int,
+                    V_total: int, stream=None) -> torch.Tensor:
+        """Per-row partial statistics [T, 4] of one vocabulary shard (columns
+        [v0, v0 + logits.shape[1]) of V_total); targets are global column numbers."""
+        a, _out, keep = self.build_args(logits, targets, loss_mask, grad=None, want=())
+        part = torch.empty((logits.shape[0], 4), dtype=torch.float32, device=logits.device)
+        st = _lib.load().lmloss_shard_stats(self.handle, a, int(v0), int(V_total), _ptr(part),
+                                            self._stream(stream))
+        if st != _lib.LMLOSS_OK:
+            raise LMLossError(st, "lmloss_shard_stats")
+        return part
+
+    def shard_merge(self, parts, targets: torch.Tensor, loss_mask=None, *, V_total: int, ce_weight: float = 1.0,
+                    z_alpha: float = 0.0, reduction: str = "token_mean", denominator: float = 1.0,
+                    want=("logp", "lse", "count"), stream=None) -> Outputs:
+        """Merge the shards' partials (a list of [T, 4] tensors, in shard order) into
+        the rows' NLL and lse and the losses; the statistics stay in the handle for
+        shard_grad."""
+        T = targets.shape[0]
+        dev = targets.device
+        _need(targets, "targets", torch.int64, T, dev)
+        if loss_mask is not None:
+            _need(loss_mask, "loss_mask", torch.uint8, T, dev)
+        for k, q in enumerate(parts):
+            _need(q, f"parts[{k}]", torch.float32, 4 * T, dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        out = Outputs(loss=torch.empty(5, **f32))
+        out.logp = torch.empty(T, **f32) if "logp" in want else None
+        out.lse = torch.empty(T, **f32) if "lse" in want else None
+        out.count = torch.empty(2, dtype=torch.int64, device=dev) if "count" in want else None
+        a = _lib.lmloss_args()
+        a.T, a.V, a.ld = T, int(V_total), int(V_total)
+        a.dtype = _lib.LMLOSS_FP32
+        a.reduction = _RED[reduction]
+        a.targets = _ptr(targets)
+        a.loss_mask = _ptr(loss_mask)
+        a.ce_weight = float(ce_weight)
+        a.z_alpha = float(z_alpha)
+        a.temperature = 1.0
+        a.denominator = float(denominator)
+        a.loss_out = _ptr(out.loss)
+        a.logp_out = _ptr(out.logp)
+        a.lse_out = _ptr(out.lse)
+        a.count_out = _ptr(out.count)
+        ptrs = (ctypes.c_void_p * len(parts))(*[_ptr(q) for q in parts])
+        st = _lib.load().lmloss_shard_merge(self.handle, a, ptrs, len(parts), self._stream(stream))
+        if st != _lib.LMLOSS_OK:
+            raise LMLossError(st, "lmloss_shard_merge")
+        return out
+
+    def shard_grad(self, logits: torch.Tensor, targets: torch.Tensor, loss_mask=None, *, v0: int, V_total: int,
+                   ce_weight: float = 1.0, z_alpha: float = 0.0, reduction: str = "token_mean",
+                   denominator: float = 1.0, grad: Union[str, torch.Tensor] = "new", stream=None) -> torch.Tensor:
+        """Gradient of one vocabulary shard from the statistics of the last shard_merge."""
+        a, out, keep = self.build_args(logits, targets, loss_mask, ce_weight=ce_weight, z_alpha=z_alpha,
+                                       reduction=reduction, denominator=denominator, grad=grad, want=())
+        st = _lib.load().lmloss_shard_grad(self.handle, a, int(v0), int(V_total), self._stream(stream))
+        if st != _lib.LMLOSS_OK:
+            raise LMLossError(st, "lmloss_shard_grad")
+        return out.grad
 
 
 def lmloss_forward_backward(logits, targets, loss_mask=None, **kw) -> Outputs:

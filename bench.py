@@ -77,18 +77,29 @@ def read_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_digest() -> str:
+    """sha256 of the kernel sources (kernels.cuh, then ptx.cuh) with comments
+    and blank lines removed: a comment edit leaves the recorded counters valid,
+    any code edit does not."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ("kernels.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "lm_head_vocab_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip()).encode())
+    return h.hexdigest()
+
+
 def read_traffic(kernel_tag: str):
     """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (same sha256), else None."""
-    import hashlib
+    the current kernel code (same kernel_source_digest), else None."""
     prof = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     if not os.path.exists(prof):
         return None
-    h = hashlib.sha256()
-    for f in ("kernels.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "lm_head_vocab_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    digest = h.hexdigest()
+    digest = kernel_source_digest()
     vals = {}
     with open(prof) as f:
         for line in f:

@@ -126,7 +126,7 @@ typedef struct {
     int32_t path;                /* 0 fused single-read, 1 stats-only, 2 GSPO three-phase  */
     int32_t cluster;             /* CTAs per row in the fused kernel                       */
     int32_t threads;             /* threads per CTA of the main kernel                     */
-    int32_t nbuf;                /* staged rows per CTA in the fused kernel                */
+    int32_t nbuf;                /* staging buffers per CTA in the fused kernel (1 or 2)   */
     int32_t grid;                /* CTAs of the main kernel                                */
     int32_t smem_bytes;          /* dynamic shared memory per CTA of the main kernel       */
     int32_t reserved;

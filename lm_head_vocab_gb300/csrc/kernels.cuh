@@ -356,15 +356,15 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 //
 // A cluster of C CTAs owns one row at a time; CTA k of the cluster owns the
 // columns [k*slice, (k+1)*slice).  Each CTA stages its slice (and the teacher
-// slice) in shared memory with one bulk copy per row, nbuf rows ahead, then
-//   pass A: maximum over its non-target columns (packed bf16x2 max),
+// slice) in shared memory with one bulk copy per row (nbuf buffers), then
+//   pass A: maximum over its non-target columns (packed bf16x2 max), per warp,
 //   pass B: sum of 2^((z - m) log2 e) over non-target columns, relative to
-//           the CTA maximum (+ teacher max, sum and cross term),
-// publishes one record per CTA, synchronises the cluster, and one warp reads
-// every CTA's record through distributed shared memory, merges them in rank
-// order and forms the row's scalars in double precision.  Pass C then writes
-// the gradient of the slice from the staged copy.  The row is read from HBM
-// once and the gradient written once.
+//           the warp's maximum (+ teacher max, sum and cross term),
+// rebases the warps' partials onto the CTA maximum, pushes one record per CTA
+// into every peer's shared memory, and one warp of every CTA merges the
+// cluster's records in rank order into the row's fp32 scalars.  Pass C then
+// writes the gradient of the slice from the staged copy.  The row is read from
+// HBM once and the gradient written once.
 //
 // Rows are handed out dynamically: rank 0 of each cluster claims the row for
 // a later iteration from a global counter and passes it to its peers in its
@@ -906,7 +906,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
         }
 
-        // ---- merge the cluster's records (one warp), row scalars in double
+        // ---- merge the cluster's records (one warp), row scalars in fp32
         if (warp == 0) {
             if (!failed && !mbar_wait_cluster_bounded(smem_addr(&rbar[i & 1]), static_cast<uint32_t>((i >> 1) & 1),
                                                       kWaitLimitCycles)) {

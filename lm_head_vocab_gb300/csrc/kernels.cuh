@@ -305,6 +305,7 @@ __device__ __forceinline__ void row_interior(const void* base, int64_t r, int64_
 __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
 {
     __shared__ long long part[8];
+    __shared__ long long fin[kRedBlocks];
     __shared__ bool last;
     const int tid = threadIdx.x, nb = gridDim.x;
     const int64_t chunk = (p.T + nb - 1) / nb;
@@ -342,12 +343,17 @@ __global__ void __launch_bounds__(256) count_kernel(const CallParams p)
         last = atomicAdd(&p.ws.done[0], 1u) == static_cast<unsigned>(nb - 1);
     }
     __syncthreads();
-    if (last && tid == 0) {
+    if (last) {
+        // the last block: the block counts are loaded in parallel, then added
         __threadfence();
-        long long tot = 0;
-        for (int k = 0; k < nb; ++k) tot += *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[k]);
-        *p.ws.n_active = tot;
-        p.ws.done[0] = 0u;
+        if (tid < nb) fin[tid] = *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[tid]);
+        __syncthreads();
+        if (tid == 0) {
+            long long tot = 0;
+            for (int k = 0; k < nb; ++k) tot += fin[k];
+            *p.ws.n_active = tot;
+            p.ws.done[0] = 0u;
+        }
     }
 }
 
@@ -1340,6 +1346,7 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
 __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
 {
     __shared__ double part[4][8];
+    __shared__ double fin[4][kRedBlocks];
     __shared__ bool last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5, nb = gridDim.x;
     const int64_t chunk = (p.T + nb - 1) / nb;
@@ -1371,12 +1378,22 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
         last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
     }
     __syncthreads();
-    if (last && tid == 0) {
-        __threadfence();
+    if (!last) return;
+    // the last block: the block partials are loaded in parallel, then one
+    // thread adds them in block order (the same order on every call)
+    __threadfence();
+    if (tid < nb) {
+        const volatile double* rp = p.ws.red_part + 4 * tid;
+        fin[0][tid] = rp[0];
+        fin[1][tid] = rp[1];
+        fin[2][tid] = rp[2];
+        fin[3][tid] = rp[3];
+    }
+    __syncthreads();
+    if (tid == 0) {
         double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
-        const volatile double* rp = p.ws.red_part;
         for (int k = 0; k < nb; ++k) {
-            sa += rp[4 * k]; sb += rp[4 * k + 1]; sc += rp[4 * k + 2]; sd += rp[4 * k + 3];
+            sa += fin[0][k]; sb += fin[1][k]; sc += fin[2][k]; sd += fin[3][k];
         }
         p.ws.done[1] = 0u;
         const int64_t n = *p.ws.n_active;

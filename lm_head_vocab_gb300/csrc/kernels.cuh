@@ -187,6 +187,7 @@ struct Workspace {
 };
 
 constexpr int kRedBlocks = 64;   // blocks of the count and reduce kernels
+static_assert(kRedBlocks % 32 == 0 && kRedBlocks <= 256, "whole warps of block partials, one block of 256 threads");
 
 // Modes of the staged-row kernel: statistics and gradient in one pass; the
 // statistics alone (forward only, and the first pass of GSPO); the gradient
@@ -1367,32 +1368,52 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
     }
     if (lane == 0) { part[0][warp] = a; part[1][warp] = b; part[2][warp] = c; part[3][warp] = d; }
     __syncthreads();
-    if (tid == 0) {
-        double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
-        for (int k = 0; k < nw; ++k) { sa += part[0][k]; sb += part[1][k]; sc += part[2][k]; sd += part[3][k]; }
-        p.ws.red_part[4 * blockIdx.x] = sa;
-        p.ws.red_part[4 * blockIdx.x + 1] = sb;
-        p.ws.red_part[4 * blockIdx.x + 2] = sc;
-        p.ws.red_part[4 * blockIdx.x + 3] = sd;
-        __threadfence();
-        last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
+    // the block's warps, then the blocks, are added by fixed-shape shuffle trees:
+    // the same order on every call, and log2 depth instead of a serial chain
+    // of double additions (a slow pipe on this GPU)
+    if (warp == 0) {
+        a = (lane < nw) ? part[0][lane] : 0.0;
+        b = (lane < nw) ? part[1][lane] : 0.0;
+        c = (lane < nw) ? part[2][lane] : 0.0;
+        d = (lane < nw) ? part[3][lane] : 0.0;
+        for (int off = 16; off > 0; off >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, off);
+            b += __shfl_xor_sync(0xffffffffu, b, off);
+            c += __shfl_xor_sync(0xffffffffu, c, off);
+            d += __shfl_xor_sync(0xffffffffu, d, off);
+        }
+        if (lane == 0) {
+            p.ws.red_part[4 * blockIdx.x] = a;
+            p.ws.red_part[4 * blockIdx.x + 1] = b;
+            p.ws.red_part[4 * blockIdx.x + 2] = c;
+            p.ws.red_part[4 * blockIdx.x + 3] = d;
+            __threadfence();
+            last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
+        }
     }
     __syncthreads();
     if (!last) return;
     // the last block: the block partials are loaded in parallel, then one
     // thread adds them in block order (the same order on every call)
     __threadfence();
-    if (tid < nb) {
-        const volatile double* rp = p.ws.red_part + 4 * tid;
-        fin[0][tid] = rp[0];
-        fin[1][tid] = rp[1];
-        fin[2][tid] = rp[2];
-        fin[3][tid] = rp[3];
+    if (tid < kRedBlocks) {
+        double v0 = 0.0, v1 = 0.0, v2 = 0.0, v3 = 0.0;
+        if (tid < nb) {
+            const volatile double* rp = p.ws.red_part + 4 * tid;
+            v0 = rp[0]; v1 = rp[1]; v2 = rp[2]; v3 = rp[3];
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+            v0 += __shfl_xor_sync(0xffffffffu, v0, off);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, off);
+            v2 += __shfl_xor_sync(0xffffffffu, v2, off);
+            v3 += __shfl_xor_sync(0xffffffffu, v3, off);
+        }
+        if (lane == 0) { fin[0][warp] = v0; fin[1][warp] = v1; fin[2][warp] = v2; fin[3][warp] = v3; }
     }
     __syncthreads();
     if (tid == 0) {
         double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
-        for (int k = 0; k < nb; ++k) {
+        for (int k = 0; k < kRedBlocks / 32; ++k) {
             sa += fin[0][k]; sb += fin[1][k]; sc += fin[2][k]; sd += fin[3][k];
         }
         p.ws.done[1] = 0u;

@@ -15,7 +15,7 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "liblmloss.so")
 HEADER = os.path.join(_ROOT, "include", "lmloss.h")
 SOURCES = ["lmloss.cu"]
-DEPENDS = ["lmloss.cu", "kernels.cuh", "ptx.cuh"]
+DEPENDS = ["lmloss.cu", "kernels.cuh", "aux_kernels.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]

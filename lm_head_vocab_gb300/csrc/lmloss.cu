@@ -11,6 +11,7 @@
 
 #include "../../include/lmloss.h"
 #include "kernels.cuh"
+#include "aux_kernels.cuh"
 
 using namespace lmloss;
 

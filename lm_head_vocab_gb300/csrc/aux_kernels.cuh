@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(256) shard_merge_kernel(const CallParams p, co
                 if (owners != 1) set_error(p.ws.err, kErrBadTarget);
                 nll = lse = __int_as_float(0x7fc00000);
             } else {
-                float lnS, sp_neg;
-                ce_scalars(M, S, zt, nll, lse, lnS, sp_neg);
+                float lnS, sp_neg, pt, pnt;
+                ce_scalars(M, S, zt, nll, lse, lnS, sp_neg, pt, pnt);
             }
         }
         p.ws.row_nll[r] = nll;

@@ -259,18 +259,24 @@ __device__ __forceinline__ int row_target(const CallParams& p, int64_t r)
 // Cross-entropy scalars of a row from its non-target maximum M, the sum
 // S = sum_{j != t} e^(z_j - M) and the target logit, in fp32 with no step
 // that cancels:  lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S,
-// NLL = softplus(d),  lse = lse_nt + softplus(-d).
+// NLL = softplus(d),  lse = lse_nt + softplus(-d),  and the target's and the
+// other columns' probabilities p_t = sigmoid(-d), p_nt = sigmoid(d).
 __device__ __forceinline__ void ce_scalars(float M, float S, float zt, float& nll, float& lse, float& lnS,
-                                           float& sp_neg)
+                                           float& sp_neg, float& pt, float& pnt)
 {
     lnS = (S == 0.f) ? -INFINITY : logf(S);
     const float d = (M - zt) + lnS;
-    // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|): one exp, one log1p
-    const float l1p = log1pf(expf(-fabsf(d)));
+    // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|) and sigmoid(+-d) from the
+    // same e^-|d|: one exp, one log1p, one division
+    const float E = expf(-fabsf(d));
+    const float l1p = log1pf(E);
     nll = fmaxf(d, 0.f) + l1p;
     sp_neg = fmaxf(-d, 0.f) + l1p;
     lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
     if (isnan(d)) lse = d;
+    const float inv = 1.f / (1.f + E);
+    pt = (d > 0.f) ? E * inv : inv;
+    pnt = (d > 0.f) ? inv : E * inv;
 }
 
 // Token scale s: 1/N_active (token mean, 0 if none) or 1/denominator (SUM).
@@ -933,10 +939,9 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     //   lse_nt = M + ln S,  d = lse_nt - z_t = (M - z_t) + ln S  (M - z_t exact),
                     //   NLL = softplus(d),  lse = lse_nt + softplus(-d)
                     const float zt = bad ? __int_as_float(0x7fc00000) : ztf;
-                    float nll, lse, lnS, sp_neg;
-                    ce_scalars(M, S, zt, nll, lse, lnS, sp_neg);
-                    const float pt = expf(-nll);
-                    const float tg = (pt < 0.25f) ? pt - 1.0f : expm1f(-nll);
+                    float nll, lse, lnS, sp_neg, pt, pnt;
+                    ce_scalars(M, S, zt, nll, lse, lnS, sp_neg, pt, pnt);
+                    const float tg = (pt < 0.25f) ? pt - 1.0f : -pnt;
                     float kl = 0.f, dlu = 0.f;
                     if (KL) {
                         // lse_u - lse = (Mu - M) + (ln Su - ln S) - softplus(-d)
@@ -986,7 +991,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                             //   H = p_t NLL + p_nt (ln S - B/S + softplus(-d)),
                             // every term non-negative (ln S - B/S is the entropy of the
                             // non-target distribution), hence no cancellation on confident rows
-                            const float pnt = -expm1f(-nll);
                             float h = (pt > 0.f) ? pt * nll : 0.f;
                             if (S > 0.f) h = fmaf(pnt, (lnS - Bc / S) + sp_neg, h);
                             p.entropy_out[r] = h;

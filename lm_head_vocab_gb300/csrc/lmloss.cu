@@ -146,8 +146,9 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     // Default shape, from sweeps on GB300: one staged row per CTA; the
     // smallest cluster whose slice (logits, plus teacher) fits in 56 KB (112 KB
     // with a teacher), so that four (two) CTAs share an SM; and about 110
-    // elements per thread (55 with a teacher, whose two CTAs per SM need more
-    // warps to hide latency), rounded to 128, 256 or 512 threads.
+    // elements per thread (55 for the gradient pass with a teacher, whose two
+    // CTAs per SM need more warps to hide latency), rounded to 128, 256 or 512
+    // threads.
     int nbuf = h->cfg_nbuf ? h->cfg_nbuf : 1;
     int C = h->cfg_cluster;
     if (!C) {
@@ -158,7 +159,7 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     }
     int NT = h->cfg_threads;
     if (!NT) {
-        const double per_thread = static_cast<double>((a->V + C - 1) / C) / (kl ? 55.0 : 110.0);
+        const double per_thread = static_cast<double>((a->V + C - 1) / C) / (kl && mode != kModeStats ? 55.0 : 110.0);
         NT = per_thread < 181.0 ? 128 : (per_thread < 362.0 ? 256 : 512);
     }
     if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel

@@ -1133,6 +1133,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
         }
     }
+    grid_dep_launch();    // the reduction after this kernel may begin launching
     cluster_sync_all();   // no CTA leaves while a peer may still read its records
 }
 

@@ -243,6 +243,29 @@ lmloss_status launch_err()
     return cudaGetLastError() == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
 }
 
+// The loss reduction, launched so that it may start while the staged-row
+// kernel before it finishes (it waits for that kernel's writes first).
+lmloss_status launch_reduce(const CallParams& p, int blocks, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    CallParams q = p;
+    void* kargs[] = {&q};
+    if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_kernel), kargs) != cudaSuccess) {
+        cudaGetLastError();
+        return LMLOSS_ERR_CUDA;
+    }
+    return LMLOSS_OK;
+}
+
 // Plan and launch the staged-row kernel in one of its modes.
 lmloss_status launch_fused(lmloss_ctx* h, const lmloss_args* a, CallParams& p, int mode, cudaStream_t stream,
                            lmloss_call_info& info)
@@ -507,8 +530,7 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
         cudaEventRecord(h->ev[2 * ev_slot + 1], stream);
         h->ev_used = ev_slot + 1;
     }
-    reduce_kernel<<<red_blocks, 256, 0, stream>>>(p);
-    if ((st = launch_err()) != LMLOSS_OK) return st;
+    if ((st = launch_reduce(p, red_blocks, stream)) != LMLOSS_OK) return st;
     info.launches += 1;
     h->info = info;
     return LMLOSS_OK;

@@ -124,6 +124,23 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank)
     return remote;
 }
 
+// ------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it on the stream still runs: it waits here, before its
+// first access to what that kernel writes, until that kernel has finished and
+// its writes are visible.  (Without that launch attribute this returns at once.)
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the kernel that follows on the stream begin launching (it still waits
+// for this one with grid_dep_wait before reading anything it writes).
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- memory
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {

@@ -157,6 +157,38 @@ def test_deterministic_repeat(dev, handle):
     assert torch.equal(a.loss, b.loss)
 
 
+def test_back_to_back_calls_match_synchronised_calls(dev, handle):
+    """Calls of different kinds queued on one stream with no host sync between
+    them (each kernel may start while the one before it finishes) give the same
+    bits as the same calls with a sync after each."""
+    cases = [_case(dev, "ce_z_bf16", dict(T=2048, V=32000)),
+             _case(dev, "gspo_z_bf16", dict(T=1024, V=151936, packed_len=256)),
+             _case(dev, "ce_z_kl_bf16", dict(T=64, V=262144)),
+             _case(dev, "confident_bf16", dict(T=512, V=128256))]
+    inps = [c.device_inputs() for c in cases]
+
+    def call(c, inp, grad):
+        return handle.forward_backward(
+            inp["logits"], inp["targets"], inp["loss_mask"], teacher_logits=inp["teacher_logits"],
+            segment_ids=inp.get("segment_ids"), advantages=inp.get("advantages"),
+            old_logprobs=inp.get("old_logprobs"), grad=grad, want=WANT, **c.kwargs())
+
+    order = [(k, g) for _ in range(2) for k in range(len(cases)) for g in ("new", None)]
+    ref = []
+    for k, g in order:
+        ref.append(call(cases[k], inps[k], g))
+        torch.cuda.synchronize()
+    got = [call(cases[k], inps[k], g) for k, g in order]
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    for (k, g), a, b in zip(order, ref, got):
+        assert torch.equal(a.loss, b.loss), (k, g)
+        assert torch.equal(a.logp, b.logp) and torch.equal(a.lse, b.lse), (k, g)
+        assert torch.equal(a.count, b.count), (k, g)
+        if g is not None:
+            assert torch.equal(a.grad.view(torch.int16), b.grad.view(torch.int16)), (k, g)
+
+
 @pytest.mark.parametrize("cluster,threads,nbuf", [(1, 256, 1), (2, 512, 2), (3, 512, 1), (4, 256, 2),
                                                   (8, 512, 2), (16, 128, 1)])
 def test_launch_shapes(dev, handle, cluster, threads, nbuf):

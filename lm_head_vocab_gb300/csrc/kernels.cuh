@@ -76,22 +76,6 @@ struct Vec<true> {
     {
         return fmaxf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
     }
-    // Running packed minimum (used to spot -inf teacher logits).
-    __device__ static __forceinline__ uint32_t min_init() { return 0x7f807f80u; }  // (+inf, +inf)
-    __device__ static __forceinline__ uint32_t min_acc(uint32_t acc, const uint4& q)
-    {
-        __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
-        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
-        __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&q.z);
-        __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&q.w);
-        __nv_bfloat162 m = __hmin2(__hmin2(a, b), __hmin2(c, d));
-        __nv_bfloat162 r = __hmin2(m, *reinterpret_cast<__nv_bfloat162*>(&acc));
-        return *reinterpret_cast<uint32_t*>(&r);
-    }
-    __device__ static __forceinline__ float min_final(uint32_t acc)
-    {
-        return fminf(__uint_as_float(acc << 16), __uint_as_float(acc & 0xffff0000u));
-    }
     // Pair k (elements 2k, 2k+1) of a vector as packed fp32.
     __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
     {
@@ -134,14 +118,6 @@ struct Vec<false> {
         return __float_as_uint(fmaxf(m, __uint_as_float(acc)));
     }
     __device__ static __forceinline__ float max_final(uint32_t acc) { return __uint_as_float(acc); }
-    __device__ static __forceinline__ uint32_t min_init() { return 0x7f800000u; }
-    __device__ static __forceinline__ uint32_t min_acc(uint32_t acc, const uint4& q)
-    {
-        float m = fminf(fminf(__uint_as_float(q.x), __uint_as_float(q.y)),
-                        fminf(__uint_as_float(q.z), __uint_as_float(q.w)));
-        return __float_as_uint(fminf(m, __uint_as_float(acc)));
-    }
-    __device__ static __forceinline__ float min_final(uint32_t acc) { return __uint_as_float(acc); }
     __device__ static __forceinline__ uint64_t pair(const uint4& q, int k)
     {
         return k == 0 ? f2_pack(__uint_as_float(q.x), __uint_as_float(q.y))
@@ -402,7 +378,8 @@ __device__ __forceinline__ void sums_plain(uint32_t bz, int nvec, int tid, int v
     b_out = b0;
 }
 
-// The same with the teacher slice (guard-free form: no teacher logit is -inf):
+// The same with the teacher slice (guard-free form: a -inf teacher logit makes
+// w NaN, and the caller then takes w again with sum_w_guarded):
 //   su = sum 2^c, c = u log2e - muL,   w = sum 2^c (u - z).
 template <class IO, int NT, bool ENT>
 __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float mL,
@@ -477,6 +454,25 @@ __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int
     return b;
 }
 
+// w = sum 2^c (u - z) over this thread's columns of the interior (the target's
+// included), skipping 2^c = 0.
+template <class IO, int NT>
+__device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, int tid, float muL)
+{
+    constexpr int VN = IO::N;
+    float w = 0.f;
+    for (int v = tid; v < nvec; v += NT) {
+        float x[VN], y[VN];
+        IO::unpack(lds128(bz + v * 16), x);
+        IO::unpack(lds128(bu + v * 16), y);
+        for (int j = 0; j < VN; ++j) {
+            const float eu = ex2(fmaf(y[j], kLog2e, -muL));
+            if (eu > 0.f) w = fmaf(eu, y[j] - x[j], w);
+        }
+    }
+    return w;
+}
+
 // Occupancy: without a teacher, shared memory admits 1024 threads per SM at the
 // default shape; with one, two CTAs share an SM, so registers are capped to fit two.
 template <bool KL, int NT>
@@ -493,6 +489,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     constexpr int ESZ = IO::ESZ;
     constexpr int NW = NT / 32;
     static_assert(NW <= 32, "at most 32 warps");
+    // butterflies over the warps' partials (lanes 0..NW-1) and over the cluster's
+    // records (lanes 0..C-1, C <= 16): lanes 0..15 already hold the full result
+    // after the rounds below 16 when at most 16 lanes carry values, and lanes
+    // 0..C-1 are the ones that use it
+    constexpr int kPubOff = NW > 16 ? 16 : 8;
+    constexpr int kRecOff = kMaxCluster / 2;
+    static_assert(kMaxCluster == 16, "record butterflies cover lanes 0..15");
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);                  // [2] staged-row copies
@@ -626,10 +629,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         // warp takes its sums against its own maxima and the warps' partials are
         // rebased once, when the CTA's record is built, so no CTA barrier sits
         // between the two passes
-        float m_w = -INFINITY, mu_w = -INFINITY, un_w = INFINITY;
+        float m_w = -INFINITY, mu_w = -INFINITY;
         if (act && mode != kModeGrad) {
-            uint32_t accz = IO::max_init(), accu = IO::max_init(), accn = IO::min_init();
-            float mx = -INFINITY, mu = -INFINITY, un = INFINITY;
+            uint32_t accz = IO::max_init(), accu = IO::max_init();
+            float mx = -INFINITY, mu = -INFINITY;
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
@@ -647,7 +650,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 if (KL) {
                     const uint4 qu = lds128(bu + v * 16);
                     accu = IO::max_acc(accu, qu);
-                    accn = IO::min_acc(accn, qu);
                 }
             }
             if (tid == NT - 1) {
@@ -660,7 +662,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             mu = fmaxf(mu, y);
-                            un = fminf(un, y);
                         }
                     }
                 }
@@ -670,15 +671,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
             if (KL) {
                 mu = fmaxf(mu, IO::max_final(accu));
-                un = fminf(un, IO::min_final(accn));
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
-                    un = fminf(un, __shfl_xor_sync(0xffffffffu, un, off));
-                }
+                for (int off = 16; off > 0; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
             }
             m_w = m;
-            if (KL) { mu_w = mu; un_w = un; }
+            if (KL) mu_w = mu;
         }
 
         // ---- pass B: sums relative to the warp's maxima
@@ -691,43 +688,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 else sums_plain<IO, NT, false>(bz, nvec, tid, vt, kt, mL, s0, b0);
             }
             if (KL) {
-                // with no -inf teacher logit in the warp's columns, e^(u-mu) (u - z)
-                // needs no guard
-                if (un_w > -INFINITY) {
-                    if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                    else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                } else {
-#pragma unroll 2
-                    for (int v = tid; v < nvec; v += NT) {
-                        float x[VN];
-                        IO::unpack(lds128(bz + v * 16), x);
-                        float e[VN];
-                        float ar[VN];
-#pragma unroll
-                        for (int j = 0; j < VN; ++j) {
-                            ar[j] = fmaf(x[j], kLog2e, -mL);
-                            e[j] = ex2(ar[j]);
-                        }
-                        if (v == vt) {
-#pragma unroll
-                            for (int j = 0; j < VN; ++j)
-                                if (j == kt) e[j] = 0.f;
-                        }
-#pragma unroll
-                        for (int j = 0; j < VN; j += 2) { s0 += e[j]; s1 += e[j + 1]; }
-#pragma unroll
-                        for (int j = 0; j < VN; ++j)
-                            if (e[j] > 0.f) b0 = fmaf(e[j], ar[j], b0);
-                        float y[VN];
-                        IO::unpack(lds128(bu + v * 16), y);
-#pragma unroll
-                        for (int j = 0; j < VN; ++j) {
-                            const float eu = ex2(fmaf(y[j], kLog2e, -muL));
-                            su += eu;
-                            w += (eu > 0.f) ? eu * (y[j] - x[j]) : 0.f;
-                        }
-                    }
-                }
+                if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
+                else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
+                // a -inf teacher logit gives 0 * -inf = NaN in the guard-free cross
+                // term: a thread that met one takes that sum again with the guard
+                if (isnan(w) && !isnan(su)) w = sum_w_guarded<IO, NT>(bz, bu, nvec, tid, muL);
             }
             float s = s0 + s1;
             if (tid == NT - 1) {
@@ -786,7 +751,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const float mw = (lane < NW) ? wred[lane] : -INFINITY;
                 m_cta = mw;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
+                for (int off = kPubOff; off > 0; off >>= 1) m_cta = fmaxf(m_cta, __shfl_xor_sync(0xffffffffu, m_cta, off));
                 const float mLc = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
                 const float mLw = (mw == -INFINITY) ? 0.f : mw * kLog2e;
                 s = (lane < NW) ? wred[64 + lane] : 0.f;
@@ -799,7 +764,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const float muw = (lane < NW) ? wred[32 + lane] : -INFINITY;
                     mu_cta = muw;
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
+                    for (int off = kPubOff; off > 0; off >>= 1)
                         mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
                     const float muLc = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
                     const float muLw = (muw == -INFINITY) ? 0.f : muw * kLog2e;
@@ -810,7 +775,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     w *= fu;
                 }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
+                for (int off = kPubOff; off > 0; off >>= 1) {
                     s += __shfl_xor_sync(0xffffffffu, s, off);
                     bc += __shfl_xor_sync(0xffffffffu, bc, off);
                     if (KL) {
@@ -819,7 +784,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     }
                 }
             }
-            // every lane holds the CTA totals and builds the same record; lane c
+            // lanes 0..15 hold the CTA totals and build the same record; lane c
             // pushes it into slot [i & 1][rank] of CTA c, whose record barrier for
             // this parity counts the bytes
             const int claim_b = __shfl_sync(0xffffffffu, claim_row, 0);
@@ -898,7 +863,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             } else if (act) {
                 float M = q.m;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                for (int off = kRecOff; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
                 const float fz = rescale(q.m, M);
                 float S = q.s * fz;
                 // sum e^(z - M) (z - M) over this CTA's non-target columns
@@ -908,13 +873,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 float Mu = q.mu, Su = 0.f, W = 0.f;
                 if (KL) {
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
+                    for (int off = kRecOff; off > 0; off >>= 1) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
                     const float f = rescale(q.mu, Mu);
                     Su = q.su * f;
                     W = q.w * f;
                 }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
+                for (int off = kRecOff; off > 0; off >>= 1) {
                     S += __shfl_xor_sync(0xffffffffu, S, off);
                     if (ent) Bc += __shfl_xor_sync(0xffffffffu, Bc, off);
                     Zt += __shfl_xor_sync(0xffffffffu, Zt, off);

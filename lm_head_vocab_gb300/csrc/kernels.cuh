@@ -240,17 +240,22 @@ __device__ __forceinline__ int row_target(const CallParams& p, int64_t r)
 __device__ __forceinline__ void ce_scalars(float M, float S, float zt, float& nll, float& lse, float& lnS,
                                            float& sp_neg, float& pt, float& pnt)
 {
-    lnS = (S == 0.f) ? -INFINITY : logf(S);
+    // ln S, e^-|d| and the reciprocal by the fast intrinsics: this chain runs
+    // on one lane while the CTA waits for it.  Their errors (ln S a few 1e-7
+    // absolute; e^-|d| within 2 + 1.2|d| ulp, under 6e-6 relative while it is a
+    // normal number) stay inside the losses' 1e-5.  log1p keeps full precision,
+    // since on a confident row the whole NLL is log1p of a tiny e^-|d|.
+    lnS = (S == 0.f) ? -INFINITY : __logf(S);
     const float d = (M - zt) + lnS;
     // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|) and sigmoid(+-d) from the
     // same e^-|d|: one exp, one log1p, one division
-    const float E = expf(-fabsf(d));
+    const float E = __expf(-fabsf(d));
     const float l1p = log1pf(E);
     nll = fmaxf(d, 0.f) + l1p;
     sp_neg = fmaxf(-d, 0.f) + l1p;
     lse = (S == 0.f) ? zt : (M + lnS) + sp_neg;
     if (isnan(d)) lse = d;
-    const float inv = 1.f / (1.f + E);
+    const float inv = __fdividef(1.f, 1.f + E);
     pt = (d > 0.f) ? E * inv : inv;
     pnt = (d > 0.f) ? inv : E * inv;
 }
@@ -850,7 +855,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     RowCoef cf;
                     const float lseL = lse * kLog2e;
                     const float lseL_err = fmaf(lse, kLog2e, -lseL);
-                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2f(fabsf(a)));
+                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - __log2f(fabsf(a)));
                     cf.neg = a < 0.f;
                     cf.lseL = lseL;
                     cf.luL = 0.f;
@@ -910,9 +915,9 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     float kl = 0.f, dlu = 0.f;
                     if (KL) {
                         // lse_u - lse = (Mu - M) + (ln Su - ln S) - softplus(-d)
-                        dlu = ((Mu - M) + (logf(Su) - lnS)) - sp_neg;
+                        dlu = ((Mu - M) + (__logf(Su) - lnS)) - sp_neg;
                         if (S == 0.f) dlu = (Mu + logf(Su)) - zt;
-                        kl = W / Su - dlu;
+                        kl = __fdividef(W, Su) - dlu;
                     }
                     const float s = s_tok;
                     const float zc = 2.f * p.alpha * lse;
@@ -932,7 +937,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const float lseL = lse * kLog2e;
                     const float lseL_err = fmaf(lse, kLog2e, -lseL);
                     // (a - a) keeps a NaN coefficient (an infinite lse) a NaN
-                    const float log2_a = a_fixed ? log2_a_fixed + (a - a) : log2f(fabsf(a));
+                    const float log2_a = a_fixed ? log2_a_fixed + (a - a) : __log2f(fabsf(a));
                     cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2_a);
                     cf.neg = a < 0.f;
                     cf.lseL = lseL;

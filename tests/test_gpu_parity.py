@@ -248,6 +248,34 @@ def _tiny_problem(dev, handle, z, t, dtype, mask=None, **kw):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_extreme_margins(dev, handle, dtype):
+    """Target margins of 20 to 130 nats.  While the NLL e^d is a normal fp32 number
+    (d above about -87) it matches the oracle to the per-row tolerance and stays
+    above 0; below that it flushes to 0 (never negative, never NaN).  The target
+    gradient is never positive."""
+    rng = np.random.default_rng(11)
+    margins = np.array([20.0, 40.0, 60.0, 70.0, 80.0, 85.0, 100.0, 130.0])
+    T, V = len(margins), 4099
+    z = rng.normal(0, 1, size=(T, V))
+    t = rng.integers(0, V, size=T)
+    for r in range(T):
+        z[r, t[r]] = z[r].max() + margins[r]
+    P, R, g_ref, out = _tiny_problem(dev, handle, z, t, dtype)
+    assert handle.device_error() == 0
+    assert rel(float(out.loss[0]), R.total) <= 1e-5
+    logp = out.logp.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(logp)) and np.all(logp <= 0.0)
+    normal = -R.logp > 1e-37
+    assert normal.sum() >= 4 and (~normal).sum() >= 1
+    np.testing.assert_allclose(logp[normal], R.logp[normal], rtol=2e-5, atol=0)
+    assert np.all(logp[normal] < 0.0)
+    assert np.all(-logp[~normal] <= 1e-37)
+    g = grad_to_f64(out.grad)
+    assert all(g[r, t[r]] <= 0.0 for r in range(T))
+    check_grad(g, g_ref, dtype == "bf16", f"margins {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 17])
 def test_small_vocab(dev, handle, dtype, V):
     rng = np.random.default_rng(V)

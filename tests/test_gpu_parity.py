@@ -189,6 +189,50 @@ def test_back_to_back_calls_match_synchronised_calls(dev, handle):
             assert torch.equal(a.grad.view(torch.int16), b.grad.view(torch.int16)), (k, g)
 
 
+@pytest.mark.parametrize("name,shape", [("ce_z_bf16", dict(T=512, V=32000)),
+                                        ("ce_z_kl_bf16", dict(T=48, V=70000))])
+def test_cuda_graph_capture_and_replay(dev, handle, name, shape):
+    """A whole call captured in a CUDA graph and replayed on new input values
+    gives the bits of direct calls on those values."""
+    case = _case(dev, name, shape)
+    inp = case.device_inputs()
+    kw = case.kwargs()
+    want = ("logp", "lse", "count")
+    x = inp["logits"].clone()
+    u = None if inp["teacher_logits"] is None else inp["teacher_logits"].clone()
+    tg = inp["targets"].clone()
+    mk = None if inp["loss_mask"] is None else inp["loss_mask"].clone()
+
+    def call():
+        return handle.forward_backward(x, tg, mk, teacher_logits=u, grad="new", want=want, **kw)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()                                   # warm-up outside the capture
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = call()
+    gen = torch.Generator(device=dev)
+    for k in range(3):
+        gen.manual_seed(100 + k)
+        x.copy_((inp["logits"].float() + torch.randn(x.shape, device=dev, generator=gen)).to(x.dtype))
+        if u is not None:
+            u.copy_((inp["teacher_logits"].float() + torch.randn(u.shape, device=dev, generator=gen)).to(u.dtype))
+        tg.copy_(torch.randint(0, case.w.V, tg.shape, device=dev, generator=gen))
+        graph.replay()
+        torch.cuda.synchronize()
+        direct = call()
+        torch.cuda.synchronize()
+        assert handle.device_error() == 0
+        assert torch.equal(captured.loss, direct.loss), k
+        assert torch.equal(captured.logp, direct.logp) and torch.equal(captured.lse, direct.lse), k
+        assert torch.equal(captured.count, direct.count), k
+        assert torch.equal(captured.grad.view(torch.int16), direct.grad.view(torch.int16)), k
+
+
 @pytest.mark.parametrize("cluster,threads,nbuf", [(1, 256, 1), (2, 512, 2), (3, 512, 1), (4, 256, 2),
                                                   (8, 512, 2), (16, 128, 1)])
 def test_launch_shapes(dev, handle, cluster, threads, nbuf):

@@ -146,7 +146,9 @@ lmloss_status lmloss_destroy(lmloss_handle handle);
 lmloss_status lmloss_check_args(const lmloss_args* args);
 
 /*
- * Loss and gradient for one batch, asynchronous on `stream`.
+ * Loss and gradient for one batch, asynchronous on `stream`.  The call makes
+ * no host synchronisation and no allocation, so it may be captured into a CUDA
+ * graph and replayed (the graph then reads whatever the captured buffers hold).
  *
  * Paths:
  *   - no GSPO, grad_out != NULL: one fused kernel reads every active row once

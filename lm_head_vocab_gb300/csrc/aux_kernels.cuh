@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
     __shared__ double part[4][8];
     __shared__ double fin[4][kRedBlocks];
     __shared__ bool last;
-    grid_dep_wait();   // launched early behind the staged-row kernel: its rows first
+    // may be launched while the staged-row kernel before it still runs: its
+    // per-row results must be complete and visible before any is read
+    grid_dep_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5, nb = gridDim.x;
     const int64_t chunk = (p.T + nb - 1) / nb;
     const int64_t r0 = blockIdx.x * chunk, r1 = min(p.T, r0 + chunk);

@@ -214,8 +214,11 @@ lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info)
  * call returns LMLOSS_ERR_INVALID_ARG before anything is launched.
  *
  * The first call on a device looks up the array's device address and the
- * device's SM limits (no allocation); make that first call before any stream
- * capture.  Every call on a device shares the one array, which keeps the last
+ * device's SM limits, and clears the array (no allocation; it synchronises
+ * that device once); make that first call before any stream capture.  The
+ * address is kept for the life of the process: after cudaDeviceReset on a
+ * device the module is reloaded elsewhere, so do not call this entry point on
+ * that device again.  Every call on a device shares the one array, which keeps the last
  * call's contents, so calls that overlap on the GPU (other streams, other host
  * threads) race and must be serialised by the caller.  Device-side data errors
  * show up only as NaN losses and gradients: there is no handle to read them from.

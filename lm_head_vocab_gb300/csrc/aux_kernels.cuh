@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(1024) seam_finish_kernel(const CallParams p)
 __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
 {
     __shared__ double part[4][8];
+    __shared__ long long npart[8];
     __shared__ double fin[4][kRedBlocks];
+    __shared__ long long nfin[kRedBlocks];
     __shared__ bool last;
     // may be launched while the staged-row kernel before it still runs: its
     // per-row results must be complete and visible before any is read
@@ -231,20 +233,24 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
     const int64_t chunk = (p.T + nb - 1) / nb;
     const int64_t r0 = blockIdx.x * chunk, r1 = min(p.T, r0 + chunk);
     double a = 0.0, b = 0.0, c = 0.0, d = 0.0;
+    long long n = 0;   // active rows, counted here too: calls under SUM run no count kernel
     for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
         const double lse = p.ws.row_lse[r];
         a += p.ws.row_nll[r];
         b += lse * lse;
         c += p.ws.row_kl[r];
         if (p.tok_adv) d += p.ws.row_pol[r];
+        int64_t t;
+        n += row_active(p, r, t) ? 1 : 0;
     }
     for (int off = 16; off > 0; off >>= 1) {
         a += __shfl_xor_sync(0xffffffffu, a, off);
         b += __shfl_xor_sync(0xffffffffu, b, off);
         c += __shfl_xor_sync(0xffffffffu, c, off);
         d += __shfl_xor_sync(0xffffffffu, d, off);
+        n += __shfl_xor_sync(0xffffffffu, n, off);
     }
-    if (lane == 0) { part[0][warp] = a; part[1][warp] = b; part[2][warp] = c; part[3][warp] = d; }
+    if (lane == 0) { part[0][warp] = a; part[1][warp] = b; part[2][warp] = c; part[3][warp] = d; npart[warp] = n; }
     __syncthreads();
     // the block's warps, then the blocks, are added by fixed-shape shuffle trees:
     // the same order on every call, and log2 depth instead of a serial chain
@@ -254,17 +260,20 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
         b = (lane < nw) ? part[1][lane] : 0.0;
         c = (lane < nw) ? part[2][lane] : 0.0;
         d = (lane < nw) ? part[3][lane] : 0.0;
+        n = (lane < nw) ? npart[lane] : 0;
         for (int off = 16; off > 0; off >>= 1) {
             a += __shfl_xor_sync(0xffffffffu, a, off);
             b += __shfl_xor_sync(0xffffffffu, b, off);
             c += __shfl_xor_sync(0xffffffffu, c, off);
             d += __shfl_xor_sync(0xffffffffu, d, off);
+            n += __shfl_xor_sync(0xffffffffu, n, off);
         }
         if (lane == 0) {
             p.ws.red_part[4 * blockIdx.x] = a;
             p.ws.red_part[4 * blockIdx.x + 1] = b;
             p.ws.red_part[4 * blockIdx.x + 2] = c;
             p.ws.red_part[4 * blockIdx.x + 3] = d;
+            p.ws.cnt_part[blockIdx.x] = n;
             __threadfence();
             last = atomicAdd(&p.ws.done[1], 1u) == static_cast<unsigned>(nb - 1);
         }
@@ -279,6 +288,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
         if (tid < nb) {
             const volatile double* rp = p.ws.red_part + 4 * tid;
             v0 = rp[0]; v1 = rp[1]; v2 = rp[2]; v3 = rp[3];
+            nfin[tid] = *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[tid]);
         }
         for (int off = 16; off > 0; off >>= 1) {
             v0 += __shfl_xor_sync(0xffffffffu, v0, off);
@@ -295,7 +305,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
             sa += fin[0][k]; sb += fin[1][k]; sc += fin[2][k]; sd += fin[3][k];
         }
         p.ws.done[1] = 0u;
-        const int64_t n = *p.ws.n_active;
+        long long n = 0;
+        for (int k = 0; k < nb; ++k) n += nfin[k];
         const double s = (p.reduction == 1) ? (n > 0 ? 1.0 / static_cast<double>(n) : 0.0) : p.inv_denominator;
         const double ce = s * sa;
         const double z = s * static_cast<double>(p.alpha) * sb;

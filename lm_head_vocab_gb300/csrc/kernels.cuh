@@ -155,10 +155,10 @@ struct Workspace {
     unsigned long long* seg_absq;  // [max_S] coarse sum of |log-ratio|, 2^-8 units
     int* seg_nonfinite;  // [max_S * 3] +inf, -inf, NaN counts
     float* seg_coef;     // [max_S] per-segment gradient coefficient kappa_i
-    int* row_counter;    // [1] dynamic row hand-out of the fused kernel
+    int* row_counter;    // [1] dynamic row hand-out of the fused kernel; 0 between calls
     long long* cnt_part; // [kRedBlocks] per-block active counts
-    double* red_part;    // [kRedBlocks * 3] per-block loss sums
-    unsigned* done;      // [2] blocks finished (count, reduce); back to 0 after each call
+    double* red_part;    // [kRedBlocks * 4] per-block loss sums
+    unsigned* done;      // [3] blocks finished (count, reduce, staged-row); back to 0 after each kernel
     int* err;            // [1]
 };
 
@@ -248,8 +248,12 @@ __device__ __forceinline__ void ce_scalars(float M, float S, float zt, float& nl
     lnS = (S == 0.f) ? -INFINITY : __logf(S);
     const float d = (M - zt) + lnS;
     // softplus(+-d) = max(+-d, 0) + log1p(e^-|d|) and sigmoid(+-d) from the
-    // same e^-|d|: one exp, one log1p, one division
-    const float E = __expf(-fabsf(d));
+    // same e^-|d|: one exp, one log1p, one division.  The fast exponential
+    // flushes results below 2^-126 (|d| above about 87.3) to 0; there the
+    // precise one keeps e^-|d| as a subnormal, so a row confident by up to
+    // about 103 nats still has a nonzero loss.
+    float E = __expf(-fabsf(d));
+    if (fabsf(d) > 87.0f) E = expf(-fabsf(d));
     const float l1p = log1pf(E);
     nll = fmaxf(d, 0.f) + l1p;
     sp_neg = fmaxf(-d, 0.f) + l1p;
@@ -842,6 +846,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
+            if (bad && rank == 0 && lane == 0 && mode != kModeGrad) set_error(p.ws.err, kErrBadTarget);
             if (act && mode == kModeGrad) {
                 if (lane == 0) {
                     // s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot)
@@ -1105,6 +1110,14 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     }
     grid_dep_launch();    // the reduction after this kernel may begin launching
     cluster_sync_all();   // no CTA leaves while a peer may still read its records
+    // the last CTA to finish returns the row counter to zero for the next launch
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&p.ws.done[2], 1u) == gridDim.x - 1) {
+            *p.ws.row_counter = 0;
+            p.ws.done[2] = 0u;
+        }
+    }
 }
 
 }  // namespace lmloss

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include <cuda_runtime.h>
@@ -138,6 +139,37 @@ size_t fused_smem(int64_t V, int C, int nbuf, bool kl, int esz, int64_t* slice_o
     return kHdrBytes + static_cast<size_t>(nbuf) * (kl ? 2 : 1) * buf;
 }
 
+// The dynamic shared-memory limit and the non-portable cluster permission are
+// attributes of a kernel function on a device, shared by every handle and host
+// thread.  They are raised once per (device, function) to the device's opt-in
+// maximum, so a call on one handle never lowers the limit under another
+// handle's launch.
+lmloss_status raise_limits(const void* fn, int device, int smem_optin)
+{
+    constexpr int kMaxEntries = 1024;
+    static std::mutex mu;
+    static const void* fns[kMaxEntries];
+    static int devs[kMaxEntries];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (fns[i] == fn && devs[i] == device) return LMLOSS_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess) {
+        cudaGetLastError();
+        return LMLOSS_ERR_CUDA;
+    }
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return LMLOSS_ERR_UNSUPPORTED;
+    }
+    if (n < kMaxEntries) {
+        fns[n] = fn;
+        devs[n] = device;
+        ++n;
+    }
+    return LMLOSS_OK;
+}
+
 lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPlan& P)
 {
     const bool bf16 = a->dtype == LMLOSS_BF16;
@@ -170,11 +202,8 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     P.NT = NT;
     P.nbuf = nbuf;
     P.smem = fused_smem(a->V, C, nbuf, kl, esz, &P.slice, &P.buf_bytes);
-    if (P.smem > static_cast<size_t>(h->smem_optin)) return LMLOSS_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(P.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(P.smem)) != cudaSuccess)
-        return LMLOSS_ERR_CUDA;
-    if (C > 8 && cudaFuncSetAttribute(P.fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return LMLOSS_ERR_UNSUPPORTED;
+    lmloss_status st = raise_limits(P.fn, h->device, h->smem_optin);
+    if (st != LMLOSS_OK) return st;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -488,9 +517,15 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     int64_t rb = (a->T + 63) / 64;
     if (rb > kRedBlocks) rb = kRedBlocks;
     const int red_blocks = rb < 1 ? 1 : static_cast<int>(rb);
-    count_kernel<<<red_blocks, 256, 0, stream>>>(p);
-    if ((st = launch_err()) != LMLOSS_OK) return st;
-    info.launches = 1;
+    // The count gives the token mean its scale before any gradient is written,
+    // and clears the GSPO accumulators.  Under SUM without GSPO nothing needs
+    // it: the staged-row kernel flags bad targets and leaves its row counter at
+    // zero, and the reduction counts the active rows itself.
+    if (gspo || a->reduction == LMLOSS_REDUCE_TOKEN_MEAN) {
+        count_kernel<<<red_blocks, 256, 0, stream>>>(p);
+        if ((st = launch_err()) != LMLOSS_OK) return st;
+        info.launches = 1;
+    }
 
     int ev_slot = -1;
     if (h->timing && h->ev_used < lmloss_ctx::kMaxTimed) {
@@ -664,8 +699,6 @@ lmloss_status lmloss_shard_grad(lmloss_handle h, const lmloss_args* a, int64_t v
 // point takes no handle: its workspace is the fixed array below, which every
 // GPU that loads this library holds until the process exits.
 // ===========================================================================
-#include <mutex>
-
 namespace {
 
 constexpr int64_t kNoAllocMaxT = LMLOSS_NOALLOC_MAX_T;
@@ -693,9 +726,9 @@ struct NoAllocLayout {
     static constexpr size_t total = err + na_align(16);
 };
 
-// The workspace itself (about 1.2 MB).  It is zero when the library loads, as
-// the block counters that must start every call at zero require; the kernels
-// return those counters to zero at the end of each call and clear the
+// The workspace itself (about 1.2 MB).  The set-up below clears it once per
+// device, so the block counters that must start every call at zero do; the
+// kernels return those counters to zero at the end of each call and clear the
 // per-call accumulators themselves at its start.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NoAllocLayout::total];
 
@@ -726,6 +759,13 @@ lmloss_status noalloc_setup(int device, NoAllocDevice** out)
         if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
             return LMLOSS_ERR_CUDA;
+        // the block counters must start at zero; the array is zero when the
+        // module loads, and clearing it here states that rather than relying on it
+        // (a synchronous memset of memory the library owns: no allocation)
+        if (cudaMemset(ptr, 0, NoAllocLayout::total) != cudaSuccess) {
+            cudaGetLastError();
+            return LMLOSS_ERR_CUDA;
+        }
         d.scratch = static_cast<unsigned char*>(ptr);
         d.ready = true;
     }

@@ -9,9 +9,10 @@ then checks what it can compute one row at a time:
     gradient < 0, the row summing to ~0) from the per-row outputs;
   * gspo_z_bf16 (32768 x 151936): the full seam (segment counts and flags
     bit-exact), the losses, and sampled rows' gradients;
-  * ce_z_kl_bf16 (65536 x 262144, student and teacher 34 GB each): sampled rows'
-    statistics and gradients against the oracle, and the total loss as the
-    deterministic reduction of the per-row outputs (a property at any size).
+  * ce_z_kl_bf16 (65536 x 262144, student and teacher 34 GB each): every row's
+    statistics (log-prob, lse, KL) and the five losses against the oracle, run
+    on each chunk of rows as it is generated (the host never holds the whole
+    68 GB), and sampled rows' gradients.
 Tolerances are the same as in test_gpu_parity.py.
 """
 import numpy as np
@@ -39,8 +40,9 @@ def _bf16(a):
     return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
 
 
-def upload(w, dev, keep_host=False):
-    """Device logits (and teacher) for workload w, generated in row chunks."""
+def upload(w, dev, keep_host=False, on_chunk=None):
+    """Device logits (and teacher) for workload w, generated in row chunks;
+    on_chunk(first_row, logits_rows, teacher_rows) sees each chunk on the host."""
     tg, mg = w.targets(), w.margins()
     L = torch.empty((w.T, w.row_stride), dtype=torch.bfloat16, device=dev)
     U = torch.empty_like(L) if w.teacher_sigma is not None else None
@@ -49,10 +51,13 @@ def upload(w, dev, keep_host=False):
         n = min(CHUNK, w.T - a)
         x = w.logits_rows(a, n, targets=tg, margins=mg)
         L[a:a + n].copy_(_bf16(x))
-        if U is not None:
-            U[a:a + n].copy_(_bf16(w.teacher_rows(a, n, x)))
+        u = w.teacher_rows(a, n, x) if U is not None else None
+        if u is not None:
+            U[a:a + n].copy_(_bf16(u))
         if host is not None:
             host[a:a + n] = x
+        if on_chunk is not None:
+            on_chunk(a, x, u)
     return L, U, host
 
 
@@ -195,21 +200,42 @@ def test_gspo_z_bf16_full(dev):
 
 def test_ce_z_kl_bf16_full(dev):
     w = workloads.get("ce_z_kl_bf16")
-    L, U, _ = upload(w, dev)
+    tg, mk = w.targets(), w.loss_mask()
+    nll, lse, kl = (np.zeros(w.T) for _ in range(3))
+    act = oracle.active_mask(tg, mk).astype(bool)
+
+    def oracle_chunk(a, x, u):
+        # the oracle's per-row statistics of this chunk, from the same host bits
+        n = len(x)
+        R = oracle.forward(oracle.Problem(logits=x, V=w.V, targets=tg[a:a + n], loss_mask=mk[a:a + n],
+                                          z_alpha=w.z_alpha, teacher=u, kl_weight=w.kl_weight,
+                                          temperature=w.temperature))
+        nll[a:a + n], lse[a:a + n], kl[a:a + n] = R.nll, R.lse, R.kl
+
+    L, U, _ = upload(w, dev, on_chunk=oracle_chunk)
     out = call(dev, w, L, U, grad="inplace")
     del U
+    # the five losses: token mean over the active rows of each term, from the
+    # oracle's fp64 per-row values
+    n = int(act.sum())
+    assert int(out.count[0]) == n == w.n_active()
+    ce = float(np.sum(nll)) / n
+    z = w.z_alpha * float(np.sum(lse * lse)) / n
+    klm = float(np.sum(kl)) / n
+    ref = [w.ce_weight * ce + z + w.kl_weight * klm, ce, z, klm, 0.0]
+    loss = out.loss.cpu().numpy().astype(np.float64)
+    for k in range(4):
+        assert rel(loss[k], ref[k]) <= 1e-5, (k, loss[k], ref[k])
+    assert loss[4] == 0.0
+    # every row's statistics
+    logp_g = out.logp.cpu().numpy().astype(np.float64)
+    lse_g = out.lse.cpu().numpy().astype(np.float64)
+    kl_g = out.kl.cpu().numpy().astype(np.float64)
+    assert np.all(logp_g[~act] == 0.0) and np.all(lse_g[~act] == 0.0) and np.all(kl_g[~act] == 0.0)
+    np.testing.assert_allclose(lse_g[act], lse[act], rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(logp_g[act], -nll[act], rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(kl_g[act], kl[act], rtol=1e-4, atol=2e-6)
+    # sampled rows' gradients
     rows = sample_rows(w)
     Rs, g, gs = sampled_oracle(w, rows)
     check_rows(out, w, rows, Rs, g, gs)
-    # the total is the fixed-order reduction of the per-row outputs
-    n = int(out.count[0])
-    assert n == w.n_active()
-    nll = -out.logp.double().cpu().numpy()
-    lse = out.lse.double().cpu().numpy()
-    kl = out.kl.double().cpu().numpy()
-    ce = nll.sum() / n
-    z = w.z_alpha * (lse * lse).sum() / n
-    klm = kl.sum() / n
-    loss = out.loss.cpu().numpy()
-    assert rel(float(loss[1]), ce) <= 1e-6 and rel(float(loss[2]), z) <= 1e-6 and rel(float(loss[3]), klm) <= 1e-6
-    assert rel(float(loss[0]), w.ce_weight * ce + z + w.kl_weight * klm) <= 1e-6

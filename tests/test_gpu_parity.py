@@ -4,9 +4,11 @@ same seeded inputs, element by element.
 Tolerances (from the arithmetic, fixed here):
   losses            relative 1e-5;
   bf16 gradients    within 1 bf16 ulp of the fp64 value (a value below 2^-126
-                    may flush to 0); where the gradient is a difference of two
-                    terms (distillation), plus 2^-17 of the terms' summed
-                    magnitude (see tests/gpu_util.py for the derivation);
+                    may flush to 0); where the definition sums terms of mixed
+                    sign (distillation's a p - b q; at the target column the CE
+                    or policy term against the z / KL term), plus 2^-17 of the
+                    terms' summed magnitude (see tests/gpu_util.py), used by at
+                    most 1e-3 of the elements;
   fp32 gradients    absolute 1e-6;
   integer outputs   bit-exact (active count, segment counts, segment flags
                     away from a clip bound, masked rows exactly 0).
@@ -73,7 +75,9 @@ def compare_all(case, out, R, g_ref, what, scale=None):
     if out.kl is not None:
         np.testing.assert_allclose(out.kl.cpu().numpy()[act], R.kl[act], rtol=1e-4, atol=2e-6)
     if out.grad is not None:
-        check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what, scale)
+        _, used = check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what, scale)
+        # the mixed-sign allowance is the exception, not the rule
+        assert used <= 1e-3 * g_ref.size, (what, used)
 
 
 SMALL = [
@@ -294,11 +298,12 @@ def _tiny_problem(dev, handle, z, t, dtype, mask=None, **kw):
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_extreme_margins(dev, handle, dtype):
     """Target margins of 20 to 130 nats.  While the NLL e^d is a normal fp32 number
-    (d above about -87) it matches the oracle to the per-row tolerance and stays
-    above 0; below that it flushes to 0 (never negative, never NaN).  The target
-    gradient is never positive."""
+    (d above about -87) it matches the oracle to the per-row tolerance; while it
+    is an fp32 subnormal (d down to about -103) it stays above 0 and within a
+    few subnormal steps of the oracle; below that it is 0 (never negative, never
+    NaN).  The target gradient is never positive."""
     rng = np.random.default_rng(11)
-    margins = np.array([20.0, 40.0, 60.0, 70.0, 80.0, 85.0, 100.0, 130.0])
+    margins = np.array([20.0, 40.0, 60.0, 70.0, 80.0, 85.0, 95.0, 100.0, 130.0])
     T, V = len(margins), 4099
     z = rng.normal(0, 1, size=(T, V))
     t = rng.integers(0, V, size=T)
@@ -308,12 +313,19 @@ def test_extreme_margins(dev, handle, dtype):
     assert handle.device_error() == 0
     assert rel(float(out.loss[0]), R.total) <= 1e-5
     logp = out.logp.cpu().numpy().astype(np.float64)
+    nll_ref = -R.logp
     assert np.all(np.isfinite(logp)) and np.all(logp <= 0.0)
-    normal = -R.logp > 1e-37
-    assert normal.sum() >= 4 and (~normal).sum() >= 1
+    normal = nll_ref >= 2.0 ** -126
+    sub = (nll_ref < 2.0 ** -126) & (nll_ref >= 2.0 ** -148)
+    under = nll_ref < 2.0 ** -150
+    assert normal.sum() >= 4 and sub.sum() >= 2 and under.sum() >= 1, (normal, sub, under)
     np.testing.assert_allclose(logp[normal], R.logp[normal], rtol=2e-5, atol=0)
     assert np.all(logp[normal] < 0.0)
-    assert np.all(-logp[~normal] <= 1e-37)
+    # subnormal NLL: nonzero, within a relative 1e-3 or four subnormal steps
+    assert np.all(logp[sub] < 0.0), (logp[sub], R.logp[sub])
+    err = np.abs(-logp[sub] - nll_ref[sub])
+    assert np.all(err <= np.maximum(1e-3 * nll_ref[sub], 4 * 2.0 ** -149)), (logp[sub], R.logp[sub])
+    assert np.all(-logp[under] <= 2.0 ** -149)
     g = grad_to_f64(out.grad)
     assert all(g[r, t[r]] <= 0.0 for r in range(T))
     check_grad(g, g_ref, dtype == "bf16", f"margins {dtype}")

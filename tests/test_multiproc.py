@@ -42,7 +42,9 @@ def _worker(rank, world, port, name, out_dir):
     import bench
     import oracle
     w = _small(name)
-    w_, x, u, t, m, n_glob, _ = bench.make_problem(w, rank, world)
+    sl = bench.RankSlice(w, rank, world)
+    x, u = sl.host_rows(w.T)
+    t, m, n_glob = sl.targets, sl.mask, sl.n_active_global
     kw = bench.call_kwargs(w, world, n_glob)
     assert kw["reduction"] == "sum" and kw["denominator"] == float(n_glob)
     P = oracle.Problem(logits=x, V=w.V, targets=t, loss_mask=m, ce_weight=w.ce_weight, z_alpha=w.z_alpha,

@@ -32,6 +32,7 @@ MUTATIONS = [
      "double nlogp = (j == k) ? l1 : (z[k] - z[j]);"),
     ("entropy_max_term_rounds_to_zero", "double nlogp = (j == k) ? l1 :", "double nlogp = (j == k) ? 0.0 :"),
     ("wrong_row_stride", "out[j] = orc_elem(dtype, base, r * ld + j);", "out[j] = orc_elem(dtype, base, r * V + j);"),
+    ("bf16_decode_wrong_shift", "[idx] << 16;", "[idx] << 15;"),
 ]
 
 
@@ -71,6 +72,7 @@ def _pins_pass():
         lambda: pins.test_entropy_confident_rows(60.0),
         lambda: pins.test_brute_force_mpmath("kl_tau2", 2, 3, dict(teacher=True, kl_weight=0.7,
                                                                     temperature=2.0, z_alpha=0.01)),
+        lambda: pins.test_bf16_inputs_match_fp32_bit_for_bit(),
     ]
     # the stride mutation only shows with ld > V
     z = np.random.default_rng(0).normal(size=(3, 8)).astype(np.float32)

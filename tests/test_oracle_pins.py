@@ -525,3 +525,82 @@ def test_entropy_confident_rows(margin):
     q = 63 * mpmath.exp(-m) / (1 + 63 * mpmath.exp(-m))
     hb = -((1 - q) * mpmath.log(1 - q) + q * mpmath.log(q / 63))
     assert H[1] == pytest.approx(float(hb), rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# bf16 inputs.  The workloads hand the oracle bf16 bit patterns; every pin
+# above feeds fp32.  A bf16 value is the upper half of the fp32 with the same
+# sign, exponent and top seven fraction bits, so each pattern below is written
+# out with the value the bf16 format gives it (sign, 8-bit exponent biased by
+# 127, 7-bit fraction; subnormals at exponent field 0).  Fed as bf16 bits, the
+# oracle must give exactly the results of the same values fed as fp32, whose
+# path the pins above fix.
+# --------------------------------------------------------------------------
+BF16_TABLE = [
+    (0x3F80, 1.0),
+    (0xC040, -3.0),
+    (0x4120, 10.0),
+    (0x4049, 3.140625),                 # 2 * (1 + 73/128)
+    (0xBF00, -0.5),
+    (0x3E80, 0.25),
+    (0x4300, 128.0),
+    (0xC2F6, -123.0),                   # -64 * (1 + 118/128)
+    (0x0001, 2.0 ** -133),              # smallest subnormal: 2^-126 * 1/128
+    (0x8001, -(2.0 ** -133)),
+    (0x007F, 127 * 2.0 ** -133),        # largest subnormal
+    (0x0080, 2.0 ** -126),              # smallest normal
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),   # largest finite
+    (0xFF7F, -(2.0 - 2.0 ** -7) * 2.0 ** 127),
+    (0x0000, 0.0),
+    (0x8000, -0.0),
+    (0xFF80, -math.inf),
+]
+
+
+def test_bf16_bits_decode_table():
+    bits = np.array([b for b, _ in BF16_TABLE], dtype=np.uint16)
+    vals = np.array([v for _, v in BF16_TABLE], dtype=np.float64)
+    got = oracle.bf16_bits_to_f64(bits)
+    assert np.array_equal(got, vals)
+    assert np.array_equal(np.signbit(got), np.signbit(vals))
+
+
+def _bf16_pair(rows):
+    """The same rows as bf16 bit patterns and as fp32 values."""
+    lut = dict(BF16_TABLE)
+    b = np.array(rows, dtype=np.uint16)
+    f = np.vectorize(lambda x: lut[int(x)])(b).astype(np.float32)
+    return b, f
+
+
+def test_bf16_inputs_match_fp32_bit_for_bit():
+    rows = [
+        [0x3F80, 0xC040, 0x4120, 0x4049, 0xBF00, 0x3E80, 0x0001, 0xFF80],
+        [0x4300, 0xC2F6, 0x0080, 0x007F, 0x8001, 0x0000, 0x8000, 0x3F80],
+        [0x7F7F, 0x3F80, 0xC040, 0x0000, 0xFF80, 0x4120, 0xBF00, 0x3E80],
+        [0xC040, 0xC2F6, 0xFF7F, 0x4049, 0x3E80, 0x0080, 0x4300, 0xBF00],
+    ]
+    # teacher: the same patterns in another order (its decode is the same routine)
+    teach = [r[3:] + r[:3] for r in rows]
+    zb, zf = _bf16_pair(rows)
+    ub, uf = _bf16_pair(teach)
+    t = np.array([2, 1, 5, 6])
+    for kw in (dict(z_alpha=1e-4), dict(z_alpha=1e-4, kl_weight=0.5)):
+        use_t = "kl_weight" in kw
+        Pb = Problem(logits=zb, V=8, targets=t, teacher=ub if use_t else None, **kw)
+        Pf = Problem(logits=zf, V=8, targets=t, teacher=uf if use_t else None, **kw)
+        Rb, gb = oracle.forward_backward(Pb, nthreads=1)
+        Rf, gf = oracle.forward_backward(Pf, nthreads=1)
+        for name in ("nll", "lse", "lse_nt", "kl"):
+            assert np.array_equal(getattr(Rb, name), getattr(Rf, name)), name
+        assert Rb.total == Rf.total
+        assert np.array_equal(gb, gf)
+        assert np.array_equal(oracle.entropy(Pb), oracle.entropy(Pf))
+    # the value check that makes the comparison mean something: row 0 against
+    # its 50-digit definition from the table's values
+    mp.dps = 50
+    z0 = [mpmath.mpf(v) if math.isfinite(v) else None for v in zf[0].astype(np.float64)]
+    terms = [mpmath.exp(v) for j, v in enumerate(z0) if j != 2 and v is not None]
+    nll = mpmath.log1p(mpmath.fsum(terms) / mpmath.exp(z0[2]))
+    Rb = oracle.forward(Problem(logits=zb[:1], V=8, targets=t[:1]))
+    assert Rb.nll[0] == pytest.approx(float(nll), rel=1e-14)

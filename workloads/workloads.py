@@ -292,20 +292,24 @@ class Workload:
 
     # ---------------------------------------------------------------- bytes
     def algorithmic_bytes(self) -> int:
-        """Bytes an ideal single pass must move: logits read once (twice for
-        GSPO, whose seam sits between the reads), teacher read once, gradient
-        written once, plus the per-row side inputs."""
+        """Bytes an ideal pass over this workload must move: every active row's
+        logits read once (twice for GSPO, whose seam sits between the reads) and
+        its teacher row once; every row's gradient written once (an inactive
+        row's is zeros, and its logits are never read); plus the per-row side
+        inputs."""
         e = self.elem_bytes
-        TV = self.T * self.V
-        reads = (2 if self.has_gspo else 1) * TV * e
+        n_act = self.n_active()
+        row = self.V * e
+        reads = (2 if self.has_gspo else 1) * n_act * row
         if self.teacher_sigma is not None:
-            reads += TV * e
+            reads += n_act * row
+        writes = self.T * row
         side = 8 * self.T
         if self.mask_via == "loss_mask":
             side += self.T
         if self.has_gspo:
             side += 4 * self.T + 4 * self.T + 4 * self.segments()[1]
-        return reads + TV * e + side
+        return reads + writes + side
 
 
 WORKLOADS = {

@@ -6,8 +6,10 @@ row's max, non-target sum, collapse-free NLL, z-loss / KL terms, the gradient
 written once, and the loss reduction.  Default workload: confident_bf16
 (T=16384 rows, V=128256, bf16, 30% of rows with a planted target margin in
 [15, 40], CE, gradient in place, token mean) -- the shape the torchtitan PR
-measured (there with V split over two GPUs).  `--also` adds the other large
-workloads at their full sizes, each timed the same way, under "also".
+measured (there with V split over two GPUs).  On one GPU the line also times
+the other large workloads at their full sizes (ce_z_bf16, gspo_z_bf16 and
+ce_z_kl_bf16, the last with 2 x 34 GB of inputs), each the same way, under
+"also" (`--also none` skips them).
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream.  Between steps, untimed: in-place workloads get their
@@ -61,7 +63,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="confident_bf16")
-    ap.add_argument("--also", default="", help="comma-separated workloads timed after the main one")
+    ap.add_argument("--also", default="auto",
+                    help="comma-separated workloads timed after the main one at their full sizes; "
+                         "'auto': the other large workloads on a single GPU, none under torchrun; 'none'")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -536,9 +540,16 @@ def run_ours(args):
 
     main = time_workload(args, args.workload, dev, world, rank, main=True)
     also = {}
-    for name in [n for n in args.also.split(",") if n and n != args.workload]:
-        r = time_workload(args, name, dev, world, rank, main=False)
-        also[name] = {k: r[k] for k in ("value", "ms_per_step", "roofline", "clocks", "config", "gpu_launches")}
+    names = args.also
+    if names == "auto":
+        names = "" if (world > 1 or args.rows) else "ce_z_bf16,gspo_z_bf16,ce_z_kl_bf16"
+    for name in [n for n in names.split(",") if n and n not in ("none", args.workload)]:
+        try:
+            r = time_workload(args, name, dev, world, rank, main=False)
+            also[name] = {k: r[k] for k in ("value", "ms_per_step", "roofline", "clocks", "config", "gpu_launches")}
+        except Exception as e:   # the main line stands on its own
+            also[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {

@@ -252,6 +252,23 @@ def test_launch_shapes(dev, handle, cluster, threads, nbuf):
         handle.set_launch_config(0, 0, 0)
 
 
+@pytest.mark.parametrize("name,shape", [("ce_z_kl_bf16", dict(T=1024, V=30000)),
+                                        ("ce_z_bf16", dict(T=2048, V=32000)),
+                                        ("confident_bf16", dict(T=2048, V=8000))])
+def test_mostly_masked_rows(dev, handle, name, shape):
+    """Nine rows in ten ignored: the persistent clusters run through long
+    stretches of rows with no statistics to exchange, where the per-row records
+    must still keep a cluster's CTAs in step (a CTA that ran two rows ahead would
+    overwrite a peer's record slot)."""
+    case = _case(dev, name, shape)
+    rng = np.random.default_rng(7)
+    case.targets[rng.random(case.w.T) < 0.9] = -100      # the oracle's Problem shares this array
+    R, g_ref, scale = oracle.forward_backward(case.P, with_scale=True)
+    _, out = run(handle, case)
+    compare_all(case, out, R, g_ref, f"{name} mostly masked", scale)
+    assert int(out.count[0]) == R.n_active < 0.2 * case.w.T
+
+
 def test_shard_sum_bitwise(dev, handle):
     """Rows split into shards, each called with SUM over the global active count,
     give the full token-mean call's gradient bit for bit, and losses that add up."""

@@ -89,8 +89,10 @@ typedef struct {
     float z_alpha;               /* z-loss alpha; 0 disables                               */
 
     const void* teacher_logits;  /* [T, ld] dtype, or NULL to disable distillation         */
-    float kl_weight;             /* weight of KL(softmax(teacher) || softmax(logits))      */
-    float temperature;           /* distillation temperature; only 1 is supported          */
+    float kl_weight;             /* weight of KL(q || p^tau), q = softmax(teacher / tau),   */
+                                 /*     p^tau = softmax(logits / tau)                      */
+    float temperature;           /* distillation temperature tau: finite and > 0 with a    */
+                                 /*     teacher (ignored without one)                      */
 
     const int32_t* segment_ids;  /* [T] GSPO segment of each row, -1 = none; NULL disables */
     int32_t num_segments;        /* segments in this call, <= the handle's max_segments    */
@@ -159,12 +161,15 @@ lmloss_status lmloss_check_args(const lmloss_args* args);
  *   - GSPO: statistics pass, segment seam, gradient pass (the seam must see
  *     every row of a segment before any gradient, so the logits are read twice)
  *     [Fast-LLM PR 552, "Approach": GSPO's backward follows its eager seam].
- * Unsupported (LMLOSS_ERR_UNSUPPORTED): temperature != 1 with a teacher;
- * teacher together with GSPO.
+ * Unsupported (LMLOSS_ERR_UNSUPPORTED): teacher together with GSPO.
  * loss_out is written on every path.  The gradient is
- *   s * (ce_weight (p - onehot) + 2 z_alpha lse p + kl_weight (p - q)) + c_r (p - onehot)
- * with s the token scale and c_r the row's GSPO coefficient; it is rounded to
- * nearest-even into dtype.
+ *   s * (ce_weight (p - onehot) + 2 z_alpha lse p + kl_weight (p^tau - q) / tau)
+ *     + c_r (p - onehot)
+ * with s the token scale, c_r the row's GSPO (or GRPO) coefficient, and the
+ * distillation term the derivative of kl_weight KL(q || p^tau) (Fast-LLM PR 552,
+ * the list of combinable losses, names distillation; read as the forward KL at
+ * temperature tau with no tau^2 factor, so tau = 1 gives kl_weight (p - q)); it
+ * is rounded to nearest-even into dtype.
  */
 lmloss_status lmloss_forward_backward(lmloss_handle handle, const lmloss_args* args, cudaStream_t stream);
 

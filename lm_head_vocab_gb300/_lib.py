@@ -5,6 +5,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import shutil
 import subprocess
 from typing import Optional
 
@@ -14,11 +15,15 @@ _CSRC = os.path.join(_PKG, "csrc")
 _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "liblmloss.so")
 HEADER = os.path.join(_ROOT, "include", "lmloss.h")
-SOURCES = ["lmloss.cu"]
-DEPENDS = ["lmloss.cu", "kernels.cuh", "aux_kernels.cuh", "ptx.cuh"]
+# (source, extra flags, object): the host code with the small kernels, and the
+# staged-row kernel's six (dtype, teacher, temperature) instantiation sets, one
+# object each so that they compile in parallel
+UNITS = [("lmloss.cu", [], "lmloss.o")] + [
+    ("fused_inst.cu", [f"-DLMLOSS_FUSED_VARIANT={k}"], f"fused_{k}.o") for k in range(6)]
+DEPENDS = ["lmloss.cu", "fused_inst.cu", "fused_entry.cuh", "kernels.cuh", "aux_kernels.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared"]
+              "-Xcompiler", "-fPIC"]
 
 LMLOSS_OK = 0
 LMLOSS_ERR_INVALID_ARG = 1
@@ -43,16 +48,35 @@ def _nvcc() -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile the CUDA library for sm_103a into the package's _build folder."""
+    """Compile the CUDA library for sm_103a into the package's _build folder:
+    every translation unit at once, then one link."""
     os.makedirs(_BUILD, exist_ok=True)
     newest = max(os.path.getmtime(os.path.join(_CSRC, f)) for f in DEPENDS)
     newest = max(newest, os.path.getmtime(HEADER))
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-o", tmp] + [os.path.join(_CSRC, s) for s in SOURCES]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    work = os.path.join(_BUILD, f"tmp{os.getpid()}")
+    os.makedirs(work, exist_ok=True)
+    objs, procs = [], []
+    try:
+        for src, extra, obj in UNITS:
+            o = os.path.join(work, obj)
+            objs.append(o)
+            cmd = [_nvcc(), *NVCC_FLAGS, *extra, "-c", "-o", o, os.path.join(_CSRC, src)]
+            procs.append((cmd, subprocess.Popen(cmd)))
+        failed = [cmd for cmd, pr in procs if pr.wait() != 0]
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = os.path.join(work, "liblmloss.so")
+        subprocess.run([_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs],
+                       check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for _, pr in procs:
+            if pr.poll() is None:
+                pr.kill()
+                pr.wait()
+        shutil.rmtree(work, ignore_errors=True)
     return LIB_PATH
 
 

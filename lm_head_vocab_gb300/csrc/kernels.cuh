@@ -134,10 +134,12 @@ struct Vec<false> {
 };
 
 // --------------------------------------------------------- softmax partials
-// (m, s): s = sum exp(x - m) over some set; m = -inf with s = 0 for the empty set.
-__device__ __forceinline__ float rescale(float m, float M)
+// (m, s): s = sum 2^((x - m) L) over some set; m = -inf with s = 0 for the empty
+// set.  L = log2 e gives s = sum exp(x - m); L = log2(e) / tau the same at the
+// temperature tau.
+__device__ __forceinline__ float rescale(float m, float M, float L = kLog2e)
 {
-    return (m == M) ? 1.0f : ex2((m - M) * kLog2e);
+    return (m == M) ? 1.0f : ex2((m - M) * L);
 }
 
 // ------------------------------------------------------------ parameters
@@ -181,6 +183,9 @@ struct CallParams {
     const uint8_t* mask;
     int64_t T, V, ld;
     float w_ce, alpha, w_kl;
+    // distillation temperature tau: 1 / tau and log2(e) / tau, each rounded once
+    // from double (used only by the instantiation for tau != 1)
+    float tau_inv, tau_l2;
     int reduction;          // 0 SUM, 1 TOKEN_MEAN
     double inv_denominator; // SUM scale
     const int32_t* seg_ids;
@@ -311,24 +316,33 @@ __device__ __forceinline__ void row_interior(const void* base, int64_t r, int64_
 constexpr int kHdrBytes = 3072;   // mbarriers, row queue, cluster records, warp scratch
 constexpr int kMaxCluster = 16;
 
-struct ClusterRec {     // one CTA's partial for the current row (32 bytes, 48 with the entropy)
+struct ClusterRec {     // one CTA's partial for the current row (32 bytes; 48 with the entropy
+                        // or a teacher)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
-    float mu, su, w;    // teacher: max, sum e^(u - mu), sum e^(u - mu) (u - z)
+    float mu, su, w;    // teacher: max, sum e^((u - mu)/tau), cross term (see ma)
     float zt;           // target logit (on the CTA that owns the target column)
     int next_row;       // rank 0: row for iteration i + depth (see fused_kernel)
     int next_t;         // rank 0: its target, or -100 when the row is inactive
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
-    float pad0, pad1, pad2;
+    float st;           // tau != 1: sum e^((z - m)/tau) over the non-target columns
+    float ma;           // teacher: max of z over all the CTA's columns, the target's included;
+                        //   w is centred: sum e^((u - mu)/tau) ((u - z) - (mu - ma))
+    float pad2;
 };
 static_assert(sizeof(ClusterRec) == 48, "record is two or three 16-byte pushes");
 
 struct RowCoef {        // the row's gradient coefficients, shared by the CTA's threads
     float cz;           // a p_j = sign(a) 2^(z_j log2e - cz)
     float cq;           // teacher: b q_j = 2^(u_j log2e - cq) when b > 0
+                        //   (tau != 1: 2^((u_j - mu) Lt - cq), Lt = log2(e) / tau)
     float lseL, luL;    // teacher: p_j = 2^(z_j log2e - lseL), q_j = 2^(u_j log2e - luL)
-    float a, b;         // teacher: g_j = a p_j - b q_j
+                        //   (tau != 1: q_j = 2^((u_j - mu) Lt - luL))
+    float a, b;         // teacher: g_j = a p_j - b q_j  (tau != 1: a p_j + b (p^tau_j - q_j))
     float gt;           // target column (teacher: minus b q_t still to apply)
     int neg;            // sign of a
+    // tau != 1: b p^tau_j = 2^((z_j - mr) Lt - ct), p^tau_j = 2^((z_j - mr) Lt - ltL),
+    // with the reference points mr (student) and mu (teacher)
+    float ct, ltL, mr, mu;
 };
 
 template <class IO, int NT>
@@ -389,17 +403,25 @@ __device__ __forceinline__ void sums_plain(uint32_t bz, int nvec, int tid, int v
 
 // The same with the teacher slice (guard-free form: a -inf teacher logit makes
 // w NaN, and the caller then takes w again with sum_w_guarded):
-//   su = sum 2^c, c = u log2e - muL,   w = sum 2^c (u - z).
-template <class IO, int NT, bool ENT>
+//   su = sum 2^c, c = u Lt - muL,   w = sum 2^c ((u - z) - cw),
+// with Lt = log2e, or log2(e) / tau at a temperature (TAU), where the student's
+// non-target sum at the temperature is taken too:  st = sum 2^(z Lt - mLt).
+// cw = mu_w - ma_w centres the cross term: a column holding both the teacher's
+// and the student's maximum adds exactly 0 to it.
+template <class IO, int NT, bool ENT, bool TAU>
 __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float mL,
-                                        float muL, float& s_out, float& su_out, float& w_out, float& b_out)
+                                        float muL, float Lt, float mLt, float cw, float& s_out, float& su_out,
+                                        float& w_out, float& b_out, float& st_out)
 {
     constexpr int VN = IO::N;
     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t Lt2 = TAU ? f2_pack(Lt, Lt) : L2;
     const uint64_t nm2 = f2_pack(-mL, -mL);
     const uint64_t nmu2 = f2_pack(-muL, -muL);
+    const uint64_t nmt2 = f2_pack(-mLt, -mLt);
+    const uint64_t ncw2 = f2_pack(-cw, -cw);
     const uint64_t neg1 = f2_pack(-1.f, -1.f);
-    uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz, accb = accz;
+    uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz, accb = accz, acct = accz;
     // one vector: the student terms of every column but lane `kill` (the
     // target's, or -1), the teacher terms of every column
     auto vec = [&](int v, int kill) {
@@ -411,16 +433,24 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
             float a0, a1, u0, u1;
             const uint64_t argz = f2_fma(xz, L2, nm2);
             f2_unpack(argz, a0, a1);
-            f2_unpack(f2_fma(xu, L2, nmu2), u0, u1);
+            f2_unpack(f2_fma(xu, Lt2, nmu2), u0, u1);
             float e0 = ex2(a0), e1 = ex2(a1);
             if (2 * k == kill) e0 = 0.f;
             if (2 * k + 1 == kill) e1 = 0.f;
             const uint64_t ez = f2_pack(e0, e1);
             accz = f2_add(accz, ez);
             if (ENT) accb = f2_fma(ez, argz, accb);
+            if (TAU) {
+                float t0, t1;
+                f2_unpack(f2_fma(xz, Lt2, nmt2), t0, t1);
+                float f0 = ex2(t0), f1 = ex2(t1);
+                if (2 * k == kill) f0 = 0.f;
+                if (2 * k + 1 == kill) f1 = 0.f;
+                acct = f2_add(acct, f2_pack(f0, f1));
+            }
             const uint64_t eu = f2_pack(ex2(u0), ex2(u1));
             accu = f2_add(accu, eu);
-            accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^(u-mu) (u - z)
+            accw = f2_fma(eu, f2_add(f2_fma(xz, neg1, xu), ncw2), accw);   // e^((u-mu)/tau) ((u - z) - cw)
         }
     };
     // the target's vector is taken out of the loop, so the loop body needs no
@@ -436,6 +466,8 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
     su_out = h0 + h1;
     f2_unpack(accw, h0, h1);
     w_out = h0 + h1;
+    f2_unpack(acct, h0, h1);
+    st_out = TAU ? h0 + h1 : 0.f;
     float b0 = 0.f;
     if (ENT) {
         f2_unpack(accb, h0, h1);
@@ -463,10 +495,11 @@ __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int
     return b;
 }
 
-// w = sum 2^c (u - z) over this thread's columns of the interior (the target's
-// included), skipping 2^c = 0.
+// w = sum 2^c ((u - z) - cw), c = u Lt - muL, over this thread's columns of
+// the interior (the target's included), skipping 2^c = 0.
 template <class IO, int NT>
-__device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, int tid, float muL)
+__device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, int tid, float muL, float Lt,
+                                            float cw)
 {
     constexpr int VN = IO::N;
     float w = 0.f;
@@ -475,8 +508,8 @@ __device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, 
         IO::unpack(lds128(bz + v * 16), x);
         IO::unpack(lds128(bu + v * 16), y);
         for (int j = 0; j < VN; ++j) {
-            const float eu = ex2(fmaf(y[j], kLog2e, -muL));
-            if (eu > 0.f) w = fmaf(eu, y[j] - x[j], w);
+            const float eu = ex2(fmaf(y[j], Lt, -muL));
+            if (eu > 0.f) w = fmaf(eu, (y[j] - x[j]) - cw, w);
         }
     }
     return w;
@@ -490,9 +523,16 @@ constexpr int fused_min_blocks() { return NT >= 1024 ? 1 : (KL ? 2 : 1024 / NT);
 // EARLY: the statistics pass (no gradient), which hands its buffer to the next
 // copy as soon as pass B is done; a separate instantiation, so that the passes
 // that write the gradient compile exactly as without it.
-template <bool BF16, bool KL, int NT, bool EARLY>
+// TAU: distillation at a temperature tau != 1 (with KL only).  The teacher's
+// exponentials take the factor log2(e) / tau, and the student's tempered
+// distribution p^tau = softmax(z / tau) is a third sum next to the cross-entropy's
+// and the teacher's, so that its gradient term w_kl (p^tau - q) / tau is a
+// third exponential in pass C.  A separate instantiation, so that tau = 1
+// compiles exactly as without it.
+template <bool BF16, bool KL, int NT, bool EARLY, bool TAU>
 __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel(const CallParams p)
 {
+    static_assert(KL || !TAU, "a temperature needs a teacher");
     using IO = Vec<BF16>;
     constexpr int VN = IO::N;
     constexpr int ESZ = IO::ESZ;
@@ -513,7 +553,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     int* tq = reinterpret_cast<int*>(smem + 48);                         // [4] its target (-100: inactive)
     float* slot = reinterpret_cast<float*>(smem + 64);                   // [1] target logit
     RowCoef* coef = reinterpret_cast<RowCoef*>(smem + 96);               // [1]
-    float* wred = reinterpret_cast<float*>(smem + 256);                  // [7][32]
+    float* wred = reinterpret_cast<float*>(smem + 256);                  // [8][32]
     ClusterRec* rec = reinterpret_cast<ClusterRec*>(smem + 1280);        // [2][kMaxCluster]
     unsigned char* bufs = smem + kHdrBytes;
 
@@ -534,12 +574,15 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     constexpr bool early = EARLY;   // launched only with mode == kModeStats
     const int depth = nbuf + (early ? 1 : 0);
     const float s_tok = token_scale(p);
-    // Kernel-wide constants of the row coefficients: b = s w_kl and, when no
-    // per-row term enters it (no z-loss, no policy term), a = s (w_ce + w_kl).
-    const float b_kl = s_tok * p.w_kl;
+    // Kernel-wide constants of the row coefficients: b = s w_kl / tau and, when
+    // no per-row term enters it (no z-loss, no policy term), a = s (w_ce + w_kl)
+    // at tau = 1 (where p^tau = p), a = s w_ce otherwise.
+    const float b_kl = s_tok * p.w_kl * (TAU ? p.tau_inv : 1.f);
     const float log2_b = (b_kl > 0.f) ? log2f(b_kl) : 0.f;
     const bool a_fixed = p.alpha == 0.f && !p.tok_adv;
-    const float log2_a_fixed = log2f(fabsf(s_tok * (p.w_ce + p.w_kl)));
+    const float log2_a_fixed = log2f(fabsf(s_tok * (p.w_ce + (TAU ? 0.f : p.w_kl))));
+    // base-2 factor of the teacher's exponentials (and of the student's at the temperature)
+    const float Lt = TAU ? p.tau_l2 : kLog2e;
     const int mode = p.mode;
 
     auto buf_addr = [&](int b, int a) -> uint32_t {
@@ -638,10 +681,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         // warp takes its sums against its own maxima and the warps' partials are
         // rebased once, when the CTA's record is built, so no CTA barrier sits
         // between the two passes
-        float m_w = -INFINITY, mu_w = -INFINITY;
+        // With a teacher, also the warp's maximum of z over all its columns (target
+        // included), ma_w: the cross term of the KL is centred on (mu_w, ma_w).
+        float m_w = -INFINITY, mu_w = -INFINITY, ma_w = -INFINITY;
         if (act && mode != kModeGrad) {
             uint32_t accz = IO::max_init(), accu = IO::max_init();
             float mx = -INFINITY, mu = -INFINITY;
+            float ztr = -INFINITY;   // the target logit, on the thread that holds it
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
@@ -651,7 +697,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 #pragma unroll
                     for (int j = 0; j < VN; ++j) {
                         if (j != kt) mx = fmaxf(mx, x[j]);
-                        else slot[0] = x[j];
+                        else { slot[0] = x[j]; ztr = x[j]; }
                     }
                 } else {
                     accz = IO::max_acc(accz, q);
@@ -667,7 +713,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
                         if (j != t) mx = fmaxf(mx, x);
-                        else slot[0] = x;
+                        else { slot[0] = x; ztr = x; }
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             mu = fmaxf(mu, y);
@@ -682,6 +728,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 mu = fmaxf(mu, IO::max_final(accu));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
+                // the thread holding the target: vt's thread, or the edge thread
+                // when the target lies in a head or tail column of this slice
+                const int hold = (vt >= 0) ? vt % NT : (owner ? NT - 1 : -1);
+                const float zh = __shfl_sync(0xffffffffu, ztr, hold & 31);
+                ma_w = (hold >= 0 && (hold >> 5) == warp) ? fmaxf(m, zh) : m;
             }
             m_w = m;
             if (KL) mu_w = mu;
@@ -690,18 +741,22 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         // ---- pass B: sums relative to the warp's maxima
         if (act && mode != kModeGrad) {
             const float mL = (m_w == -INFINITY) ? 0.f : m_w * kLog2e;
-            const float muL = (mu_w == -INFINITY) ? 0.f : mu_w * kLog2e;
-            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f;
+            const float muL = (mu_w == -INFINITY) ? 0.f : mu_w * Lt;
+            const float mLt = (!TAU || m_w == -INFINITY) ? 0.f : m_w * Lt;
+            const float cw = (mu_w == -INFINITY || ma_w == -INFINITY) ? 0.f : mu_w - ma_w;
+            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f, st = 0.f;
             if (!KL) {
                 if (p.entropy_out) sums_plain<IO, NT, true>(bz, nvec, tid, vt, kt, mL, s0, b0);
                 else sums_plain<IO, NT, false>(bz, nvec, tid, vt, kt, mL, s0, b0);
             }
             if (KL) {
-                if (p.entropy_out) sums_kl<IO, NT, true>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
-                else sums_kl<IO, NT, false>(bz, bu, nvec, tid, vt, kt, mL, muL, s0, su, w, b0);
+                if (p.entropy_out)
+                    sums_kl<IO, NT, true, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, cw, s0, su, w, b0, st);
+                else
+                    sums_kl<IO, NT, false, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, cw, s0, su, w, b0, st);
                 // a -inf teacher logit gives 0 * -inf = NaN in the guard-free cross
                 // term: a thread that met one takes that sum again with the guard
-                if (isnan(w) && !isnan(su)) w = sum_w_guarded<IO, NT>(bz, bu, nvec, tid, muL);
+                if (isnan(w) && !isnan(su)) w = sum_w_guarded<IO, NT>(bz, bu, nvec, tid, muL, Lt, cw);
             }
             float s = s0 + s1;
             if (tid == NT - 1) {
@@ -714,12 +769,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                             const float e = ex2(a);
                             s += e;
                             if (e > 0.f) b0 = fmaf(e, a, b0);
+                            if (TAU) st += ex2(fmaf(x, Lt, -mLt));
                         }
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
-                            const float eu = ex2(fmaf(y, kLog2e, -muL));
+                            const float eu = ex2(fmaf(y, Lt, -muL));
                             su += eu;
-                            w += (eu > 0.f) ? eu * (y - x) : 0.f;
+                            w += (eu > 0.f) ? eu * ((y - x) - cw) : 0.f;
                         }
                     }
                 }
@@ -732,12 +788,14 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     su += __shfl_xor_sync(0xffffffffu, su, off);
                     w += __shfl_xor_sync(0xffffffffu, w, off);
                 }
+                if (TAU) st += __shfl_xor_sync(0xffffffffu, st, off);
             }
             if (lane == 0) {
                 wred[warp] = m_w;
                 wred[64 + warp] = s;
                 wred[192 + warp] = b0;
-                if (KL) { wred[32 + warp] = mu_w; wred[96 + warp] = su; wred[128 + warp] = w; }
+                if (KL) { wred[32 + warp] = mu_w; wred[96 + warp] = su; wred[128 + warp] = w; wred[224 + warp] = ma_w; }
+                if (TAU) wred[160 + warp] = st;
             }
         }
         __syncthreads();
@@ -752,8 +810,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 
         // ---- publish this CTA's record
         if (warp == 0) {
-            float s = 0.f, su = 0.f, w = 0.f, bc = 0.f;
-            float m_cta = -INFINITY, mu_cta = -INFINITY;
+            float s = 0.f, su = 0.f, w = 0.f, bc = 0.f, st = 0.f;
+            float m_cta = -INFINITY, mu_cta = -INFINITY, ma_cta = -INFINITY;
             if (act) {
                 // warp w's sums are against round(m_w log2e): rebase them onto
                 // round(m_cta log2e) (entropy partial: e (a + d) summed = f (b + s d))
@@ -769,19 +827,36 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const float fz = (s == 0.f) ? 0.f : ex2(dz);
                 bc = (s == 0.f) ? 0.f : fz * fmaf(s, dz, bc);
                 s *= fz;
+                if (TAU) {
+                    // the tempered sum likewise, against round(m Lt)
+                    st = (lane < NW) ? wred[160 + lane] : 0.f;
+                    const float mLtc = (m_cta == -INFINITY) ? 0.f : m_cta * Lt;
+                    const float mLtw = (mw == -INFINITY) ? 0.f : mw * Lt;
+                    st = (st == 0.f) ? 0.f : st * ex2(mLtw - mLtc);
+                }
                 if (KL) {
                     const float muw = (lane < NW) ? wred[32 + lane] : -INFINITY;
                     mu_cta = muw;
 #pragma unroll
                     for (int off = kPubOff; off > 0; off >>= 1)
                         mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
-                    const float muLc = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
-                    const float muLw = (muw == -INFINITY) ? 0.f : muw * kLog2e;
+                    const float maw = (lane < NW) ? wred[224 + lane] : -INFINITY;
+                    ma_cta = maw;
+#pragma unroll
+                    for (int off = kPubOff; off > 0; off >>= 1)
+                        ma_cta = fmaxf(ma_cta, __shfl_xor_sync(0xffffffffu, ma_cta, off));
+                    const float muLc = (mu_cta == -INFINITY) ? 0.f : mu_cta * Lt;
+                    const float muLw = (muw == -INFINITY) ? 0.f : muw * Lt;
                     su = (lane < NW) ? wred[96 + lane] : 0.f;
                     w = (lane < NW) ? wred[128 + lane] : 0.f;
                     const float fu = (su == 0.f) ? 0.f : ex2(muLw - muLc);
+                    // re-centre the cross term from (mu_w, ma_w) onto (mu_cta, ma_cta):
+                    // w + su ((mu_w - ma_w) - (mu_cta - ma_cta)), whose correction is
+                    // exactly 0 for the warp that holds both maxima
+                    const float cwv = (muw == -INFINITY || maw == -INFINITY) ? 0.f : muw - maw;
+                    const float cc = (mu_cta == -INFINITY || ma_cta == -INFINITY) ? 0.f : mu_cta - ma_cta;
+                    w = (su == 0.f) ? 0.f : fu * fmaf(su, cwv - cc, w);
                     su *= fu;
-                    w *= fu;
                 }
 #pragma unroll
                 for (int off = kPubOff; off > 0; off >>= 1) {
@@ -791,6 +866,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         su += __shfl_xor_sync(0xffffffffu, su, off);
                         w += __shfl_xor_sync(0xffffffffu, w, off);
                     }
+                    if (TAU) st += __shfl_xor_sync(0xffffffffu, st, off);
                 }
             }
             // lanes 0..15 hold the CTA totals and build the same record; lane c
@@ -801,7 +877,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             ClusterRec R;
             // the sums were taken against round(m log2e); undo that rounding exactly
             const float mL = (m_cta == -INFINITY) ? 0.f : m_cta * kLog2e;
-            const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * kLog2e;
+            const float muL = (mu_cta == -INFINITY) ? 0.f : mu_cta * Lt;
             R.m = m_cta;
             // e = 2^(z log2e - mL) = e^(z - m) 2^delta and bc sums e (z log2e - mL), so
             // sum e^(z - m) (z - m) = 2^-delta (bc - delta s) / log2e
@@ -809,9 +885,15 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const float f = ex2(-delta);
             R.s = s * f;
             R.bc = (bc - delta * s) * f * (1.0f / kLog2e);
-            R.pad0 = R.pad1 = R.pad2 = 0.f;
+            R.st = 0.f;
+            if (TAU) {
+                const float mLt = (m_cta == -INFINITY) ? 0.f : m_cta * Lt;
+                R.st = st * ((m_cta == -INFINITY) ? 1.f : ex2(-fmaf(m_cta, Lt, -mLt)));
+            }
+            R.ma = ma_cta;
+            R.pad2 = 0.f;
             R.mu = mu_cta;
-            const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, kLog2e, -muL));
+            const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, Lt, -muL));
             R.su = su * fu;
             R.w = w * fu;
             R.zt = owner ? slot[0] : 0.f;   // exactly 0 in every CTA but the target's owner
@@ -820,8 +902,9 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const uint4* Rv = reinterpret_cast<const uint4*>(&R);
             const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
             const uint32_t my_bar = smem_addr(&rbar[i & 1]);
-            // the entropy partial travels only when the entropy is wanted
-            const bool ent = p.entropy_out != nullptr;
+            // the third 16 bytes (entropy partial; with a teacher the all-column
+            // maximum and the tempered sum) travel only when used
+            const bool ent = KL || p.entropy_out != nullptr;
             const uint32_t rec_bytes = ent ? 48u : 32u;
             if (lane == 0) mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C) * rec_bytes);
             if (lane < C) {
@@ -842,7 +925,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
             ClusterRec q;
             q.m = -INFINITY; q.s = 0.f; q.mu = -INFINITY; q.su = 0.f; q.w = 0.f; q.zt = 0.f;
-            q.next_row = 0; q.next_t = -100; q.bc = 0.f;
+            q.next_row = 0; q.next_t = -100; q.bc = 0.f; q.st = 0.f; q.ma = -INFINITY;
             if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
@@ -867,6 +950,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     cf.a = a;
                     cf.b = 0.f;
                     cf.cq = INFINITY;
+                    cf.ct = INFINITY;
+                    cf.ltL = 0.f;
+                    cf.mr = 0.f;
+                    cf.mu = 0.f;
                     cf.gt = (s * p.w_ce + g_cr) * tg + s * zc * pt;
                     *coef = cf;
                 }
@@ -880,13 +967,20 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const bool ent = p.entropy_out != nullptr;
                 float Bc = (!ent || q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
                 float Zt = q.zt;   // summed below: every record but the owner's holds exactly 0
-                float Mu = q.mu, Su = 0.f, W = 0.f;
+                float Mu = q.mu, Su = 0.f, W = 0.f, Ma = q.ma;
+                float St = TAU ? q.st * rescale(q.m, M, Lt) : 0.f;
                 if (KL) {
 #pragma unroll
-                    for (int off = kRecOff; off > 0; off >>= 1) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
-                    const float f = rescale(q.mu, Mu);
+                    for (int off = kRecOff; off > 0; off >>= 1) {
+                        Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
+                        Ma = fmaxf(Ma, __shfl_xor_sync(0xffffffffu, Ma, off));
+                    }
+                    const float f = rescale(q.mu, Mu, Lt);
                     Su = q.su * f;
-                    W = q.w * f;
+                    // the cross term re-centred on the row's (Mu, Ma), as for the CTA's record
+                    const float cr = (q.mu == -INFINITY || q.ma == -INFINITY) ? 0.f : q.mu - q.ma;
+                    const float cM = (Mu == -INFINITY || Ma == -INFINITY) ? 0.f : Mu - Ma;
+                    W = (q.su == 0.f) ? 0.f : f * fmaf(q.su, cr - cM, q.w);
                 }
 #pragma unroll
                 for (int off = kRecOff; off > 0; off >>= 1) {
@@ -897,6 +991,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         Su += __shfl_xor_sync(0xffffffffu, Su, off);
                         W += __shfl_xor_sync(0xffffffffu, W, off);
                     }
+                    if (TAU) St += __shfl_xor_sync(0xffffffffu, St, off);
                 }
                 const float ztf = Zt;
                 if (p.part_out) {
@@ -917,12 +1012,39 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     float nll, lse, lnS, sp_neg, pt, pnt;
                     ce_scalars(M, S, zt, nll, lse, lnS, sp_neg, pt, pnt);
                     const float tg = (pt < 0.25f) ? pt - 1.0f : -pnt;
-                    float kl = 0.f, dlu = 0.f;
-                    if (KL) {
-                        // lse_u - lse = (Mu - M) + (ln Su - ln S) - softplus(-d)
-                        dlu = ((Mu - M) + (__logf(Su) - lnS)) - sp_neg;
-                        if (S == 0.f) dlu = (Mu + logf(Su)) - zt;
-                        kl = __fdividef(W, Su) - dlu;
+                    // KL = sum q (log q - log p^tau) with log q_j = (u_j - Mu)/tau - ln Su
+                    // and log p^tau_j = (z_j - Ma)/tau - (lse_tau - Ma/tau), Ma = max(M, z_t):
+                    //   KL = E_q[(u - Mu) - (z - Ma)] / tau - ln Su + (lse_tau - Ma/tau),
+                    // with the cross term W / Su = E_q[(u - Mu) - (z - Ma)] centred so
+                    // that the column holding both maxima adds exactly 0, and
+                    // lse_tau - Ma/tau = softplus(dT) when z_t >= M, rb otherwise (below):
+                    // no term grows with the logits' offset, so a small KL (both
+                    // distributions confident on one column) keeps its digits.
+                    float kl = 0.f;
+                    // tau != 1: the tempered student p^tau = softmax(z / tau) has
+                    //   lse_tau = logaddexp(z_t / tau, M / tau + ln St) = mr / tau + rb
+                    // with the reference point mr = M (z_t when no other column is
+                    // finite) and, as for the cross-entropy, dT = (M - z_t) / tau + ln St,
+                    // rb = ln St + softplus(-dT), p^tau_t = sigmoid(-dT)
+                    float mr = 0.f, rb = 0.f, ptt = 0.f, lnSu = 0.f;
+                    if (KL) lnSu = logf(Su);
+                    if (TAU) {
+                        const float lnSt = (St == 0.f) ? -INFINITY : logf(St);
+                        const float dT = fmaf(p.tau_inv, M - zt, lnSt);
+                        float E = __expf(-fabsf(dT));
+                        if (fabsf(dT) > 87.0f) E = expf(-fabsf(dT));
+                        const float l1p = log1pf(E);
+                        const float inv = __fdividef(1.f, 1.f + E);
+                        ptt = (dT > 0.f) ? E * inv : inv;
+                        mr = (St == 0.f) ? zt : M;
+                        rb = (St == 0.f) ? 0.f : lnSt + (fmaxf(-dT, 0.f) + l1p);
+                        if (isnan(dT)) rb = dT;
+                        const float lseMa = (St == 0.f || zt >= M) ? fmaxf(dT, 0.f) + l1p : rb;
+                        kl = fmaf(__fdividef(W, Su), p.tau_inv, lseMa - lnSu);
+                    } else if (KL) {
+                        // lse - Ma: NLL when the target is the maximum, else ln S + softplus(-d)
+                        const float lseMa = (S == 0.f || zt >= M) ? nll : lnS + sp_neg;
+                        kl = __fdividef(W, Su) + (lseMa - lnSu);
                     }
                     const float s = s_tok;
                     const float zc = 2.f * p.alpha * lse;
@@ -936,7 +1058,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         if (rho * g_adv <= rc * g_adv) c_r = s * g_adv * rho;
                         if (isnan(rho) || isnan(g_adv)) { pol = rho + g_adv; c_r = pol; }
                     }
-                    const float a = s * (p.w_ce + zc + p.w_kl) + c_r;
+                    const float a = s * (p.w_ce + zc + (TAU ? 0.f : p.w_kl)) + c_r;
                     RowCoef cf;
                     // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
                     const float lseL = lse * kLog2e;
@@ -946,13 +1068,30 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2_a);
                     cf.neg = a < 0.f;
                     cf.lseL = lseL;
-                    const float lu = lse + dlu;
-                    const float luL = lu * kLog2e;
-                    cf.luL = luL;
                     cf.a = a;
                     cf.b = b_kl;
-                    cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;
-                    cf.gt = (s * p.w_ce + c_r) * tg + s * (zc + p.w_kl) * pt;
+                    if (TAU) {
+                        // b p^tau_j = 2^((z_j - mr) Lt - ct), b q_j = 2^((u_j - Mu) Lt - cq): the
+                        // exponent offsets stay small, and the products with log2 e exact
+                        const float rbL = rb * kLog2e, raL = lnSu * kLog2e;
+                        cf.ltL = rbL;
+                        cf.luL = raL;
+                        cf.ct = (b_kl > 0.f) ? rbL + (fmaf(rb, kLog2e, -rbL) - log2_b) : INFINITY;
+                        cf.cq = (b_kl > 0.f) ? raL + (fmaf(lnSu, kLog2e, -raL) - log2_b) : INFINITY;
+                        cf.mr = mr;
+                        cf.mu = Mu;
+                        cf.gt = (s * p.w_ce + c_r) * tg + s * zc * pt + b_kl * ptt;
+                    } else {
+                        const float lu = Mu + lnSu;   // teacher's logsumexp
+                        const float luL = lu * kLog2e;
+                        cf.luL = luL;
+                        cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;
+                        cf.ct = INFINITY;
+                        cf.ltL = 0.f;
+                        cf.mr = 0.f;
+                        cf.mu = 0.f;
+                        cf.gt = (s * p.w_ce + c_r) * tg + s * (zc + p.w_kl) * pt;
+                    }
                     *coef = cf;
                     if (rank == 0) {
                         p.ws.row_nll[r] = nll;
@@ -1005,7 +1144,67 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 continue;
             }
             const RowCoef cf = *coef;
-            if (KL && cf.a > 0.f && cf.b > 0.f) {
+            if (TAU && !cf.neg && cf.b > 0.f) {
+                // g_j = 2^(z_j log2e - cz) + 2^((z_j - mr) Lt - ct) - 2^((u_j - mu) Lt - cq)
+                const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+                const uint64_t Lt2 = f2_pack(Lt, Lt);
+                const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
+                const uint64_t nct = f2_pack(-cf.ct, -cf.ct);
+                const uint64_t ncq = f2_pack(-cf.cq, -cf.cq);
+                const uint64_t nmr = f2_pack(-cf.mr, -cf.mr);
+                const uint64_t nmu = f2_pack(-cf.mu, -cf.mu);
+                const uint64_t neg1 = f2_pack(-1.f, -1.f);
+                auto vec = [&](int v, int tcol) {
+                    const uint4 q = lds128(bz + v * 16);
+                    const uint4 qu = lds128(bu + v * 16);
+                    float gv[VN];
+#pragma unroll
+                    for (int k = 0; k < VN / 2; ++k) {
+                        const uint64_t xz = IO::pair(q, k);
+                        float a0, a1, t0, t1, b0, b1;
+                        f2_unpack(f2_fma(xz, L2, ncz), a0, a1);
+                        f2_unpack(f2_fma(f2_add(xz, nmr), Lt2, nct), t0, t1);
+                        f2_unpack(f2_fma(f2_add(IO::pair(qu, k), nmu), Lt2, ncq), b0, b1);
+                        const uint64_t bq = f2_pack(ex2(b0), ex2(b1));
+                        const uint64_t ap = f2_add(f2_pack(ex2(a0), ex2(a1)), f2_pack(ex2(t0), ex2(t1)));
+                        float g0, g1;
+                        f2_unpack(f2_fma(bq, neg1, ap), g0, g1);
+                        if (tcol >= 0) {
+                            float q0, q1;
+                            f2_unpack(bq, q0, q1);
+                            if (2 * k == tcol) g0 = cf.gt - q0;
+                            if (2 * k + 1 == tcol) g1 = cf.gt - q1;
+                        }
+                        gv[2 * k] = g0;
+                        gv[2 * k + 1] = g1;
+                    }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                };
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT)
+                    if (v != vt) vec(v, -1);
+                if (vt >= 0 && vt % NT == tid) vec(vt, kt);
+            } else if (TAU) {
+                // a < 0 or b <= 0: g_j = a p_j + b (p^tau_j - q_j)
+#pragma unroll 2
+                for (int v = tid; v < nvec; v += NT) {
+                    float x[VN], y[VN], gv[VN], qv[VN];
+                    IO::unpack(lds128(bz + v * 16), x);
+                    IO::unpack(lds128(bu + v * 16), y);
+#pragma unroll
+                    for (int j = 0; j < VN; ++j) {
+                        qv[j] = cf.b * ex2(fmaf(y[j] - cf.mu, Lt, -cf.luL));
+                        const float ptj = ex2(fmaf(x[j] - cf.mr, Lt, -cf.ltL));
+                        gv[j] = fmaf(cf.a, ex2(fmaf(x[j], kLog2e, -cf.lseL)), fmaf(cf.b, ptj, -qv[j]));
+                    }
+                    if (v == vt) {
+#pragma unroll
+                        for (int j = 0; j < VN; ++j)
+                            if (j == kt) gv[j] = cf.gt - qv[j];
+                    }
+                    stg128(g + static_cast<size_t>(v) * 16, IO::pack(gv));
+                }
+            } else if (KL && cf.a > 0.f && cf.b > 0.f) {
                 // g_j = 2^(z_j log2e - cz) - 2^(u_j log2e - cq): both coefficients in the exponents
                 const uint64_t L2 = f2_pack(kLog2e, kLog2e);
                 const uint64_t ncz = f2_pack(-cf.cz, -cf.cz);
@@ -1095,7 +1294,13 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
                         float gj;
-                        if (KL) {
+                        if (TAU) {
+                            const float y = IO::load1(p.teacher, r * p.ld + j);
+                            const float qj = cf.b * ex2(fmaf(y - cf.mu, Lt, -cf.luL));
+                            const float ptj = ex2(fmaf(x - cf.mr, Lt, -cf.ltL));
+                            gj = (j == t) ? cf.gt - qj
+                                          : fmaf(cf.a, ex2(fmaf(x, kLog2e, -cf.lseL)), fmaf(cf.b, ptj, -qj));
+                        } else if (KL) {
                             const float qj = cf.b * ex2(fmaf(IO::load1(p.teacher, r * p.ld + j), kLog2e, -cf.luL));
                             gj = (j == t) ? cf.gt - qj : fmaf(cf.a, ex2(fmaf(x, kLog2e, -cf.lseL)), -qj);
                         } else {

@@ -13,6 +13,7 @@
 #include "../../include/lmloss.h"
 #include "kernels.cuh"
 #include "aux_kernels.cuh"
+#include "fused_entry.cuh"
 
 using namespace lmloss;
 
@@ -78,8 +79,8 @@ lmloss_status check(const lmloss_args* a, bool need_loss = true)
     if (a->grad_out && a->T > 0 && misaligned(a->grad_out, a->logits)) return LMLOSS_ERR_INVALID_ARG;
     if (a->teacher_logits) {
         if (a->T > 0 && misaligned(a->teacher_logits, a->logits)) return LMLOSS_ERR_INVALID_ARG;
-        if (!std::isfinite(a->kl_weight) || !(a->temperature > 0.f)) return LMLOSS_ERR_INVALID_ARG;
-        if (a->temperature != 1.0f) return LMLOSS_ERR_UNSUPPORTED;
+        if (!std::isfinite(a->kl_weight) || !(a->temperature > 0.f) || !std::isfinite(a->temperature))
+            return LMLOSS_ERR_INVALID_ARG;
         if (a->grad_out == a->teacher_logits) return LMLOSS_ERR_INVALID_ARG;
     }
     if (a->segment_ids) {
@@ -98,26 +99,15 @@ lmloss_status check(const lmloss_args* a, bool need_loss = true)
 }
 
 // ------------------------------------------------------------ launch plans
-template <bool BF16, bool KL, int NT>
-const void* fused_ptr(bool stats)
+// tau: distillation at a temperature other than 1 (kl only)
+const void* pick_fused(bool bf16, bool kl, bool tau, int nt, bool stats)
 {
-    return stats ? reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT, true>)
-                 : reinterpret_cast<const void*>(&fused_kernel<BF16, KL, NT, false>);
-}
-
-const void* pick_fused(bool bf16, bool kl, int nt, bool stats)
-{
-#define LMLOSS_PICK(NTV)                                                                          \
-    if (nt == NTV) {                                                                              \
-        if (bf16) return kl ? fused_ptr<true, true, NTV>(stats) : fused_ptr<true, false, NTV>(stats); \
-        return kl ? fused_ptr<false, true, NTV>(stats) : fused_ptr<false, false, NTV>(stats);      \
+    if (bf16) {
+        if (!kl) return fused_entry<true, false, false>(nt, stats);
+        return tau ? fused_entry<true, true, true>(nt, stats) : fused_entry<true, true, false>(nt, stats);
     }
-    LMLOSS_PICK(128)
-    LMLOSS_PICK(256)
-    LMLOSS_PICK(512)
-    LMLOSS_PICK(1024)
-#undef LMLOSS_PICK
-    return nullptr;
+    if (!kl) return fused_entry<false, false, false>(nt, stats);
+    return tau ? fused_entry<false, true, true>(nt, stats) : fused_entry<false, true, false>(nt, stats);
 }
 
 struct FusedPlan {
@@ -196,7 +186,7 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     }
     if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel
     if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
-    P.fn = pick_fused(bf16, kl, NT, mode == kModeStats);
+    P.fn = pick_fused(bf16, kl, kl && a->temperature != 1.0f, NT, mode == kModeStats);
     if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
     P.C = C;
     P.NT = NT;
@@ -242,6 +232,9 @@ void fill_params(const lmloss_ctx* h, const lmloss_args* a, CallParams& p)
     p.w_ce = a->ce_weight;
     p.alpha = a->z_alpha;
     p.w_kl = kl ? a->kl_weight : 0.f;
+    // 1 / tau and log2(e) / tau, each rounded once
+    p.tau_inv = kl ? static_cast<float>(1.0 / static_cast<double>(a->temperature)) : 1.f;
+    p.tau_l2 = kl ? static_cast<float>(1.4426950408889634 / static_cast<double>(a->temperature)) : kLog2e;
     p.reduction = a->reduction;
     p.inv_denominator = a->reduction == LMLOSS_REDUCE_SUM ? 1.0 / a->denominator : 0.0;
     p.seg_ids = a->segment_ids;

@@ -9,6 +9,7 @@ import oracle
 import workloads
 
 BF16_TINY = 2.0 ** -126
+WANT = ("logp", "lse", "kl", "count", "seg")
 
 
 def to_device(x: np.ndarray, dev) -> torch.Tensor:
@@ -120,10 +121,49 @@ class Case:
 
     def kwargs(self):
         w = self.w
-        kw = dict(ce_weight=w.ce_weight, z_alpha=w.z_alpha, kl_weight=w.kl_weight,
+        # V: the workload's columns (the device rows are [T, ld], padding beyond V)
+        kw = dict(V=w.V, ce_weight=w.ce_weight, z_alpha=w.z_alpha, kl_weight=w.kl_weight,
                   temperature=w.temperature,
                   reduction="sum" if w.reduction == "sum_active" else "token_mean",
                   denominator=w.denominator())
         if w.has_gspo:
             kw.update(num_segments=self.S, clip_eps_low=w.clip_eps_low, clip_eps_high=w.clip_eps_high)
         return kw
+
+
+def run(handle, case, grad="new", inp=None):
+    inp = inp or case.device_inputs()
+    kw = case.kwargs()
+    out = handle.forward_backward(
+        inp["logits"], inp["targets"], inp["loss_mask"], teacher_logits=inp["teacher_logits"],
+        segment_ids=inp.get("segment_ids"), advantages=inp.get("advantages"),
+        old_logprobs=inp.get("old_logprobs"), grad=grad, want=WANT, **kw)
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    return inp, out
+
+
+def compare_all(case, out, R, g_ref, what, scale=None):
+    bf16 = case.w.dtype == "bf16"
+    loss = out.loss.cpu().numpy().astype(np.float64)
+    ref = [R.total, R.ce, R.z, R.kl_loss, R.gspo]
+    for k, name in enumerate(["total", "ce", "z", "kl", "gspo"]):
+        if ref[k] == 0.0:
+            assert abs(loss[k]) <= 1e-30, (what, name, loss[k])
+        else:
+            assert rel(loss[k], ref[k]) <= 1e-5, (what, name, loss[k], ref[k])
+    cnt = out.count.cpu().numpy()
+    assert cnt[0] == R.n_active
+    act = R.active.astype(bool)
+    logp = out.logp.cpu().numpy().astype(np.float64)
+    lse = out.lse.cpu().numpy().astype(np.float64)
+    assert np.all(logp[~act] == 0.0) and np.all(lse[~act] == 0.0)
+    # per-row diagnostics
+    np.testing.assert_allclose(lse[act], R.lse[act], rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(logp[act], R.logp[act], rtol=2e-5, atol=1e-6)
+    if out.kl is not None:
+        np.testing.assert_allclose(out.kl.cpu().numpy()[act], R.kl[act], rtol=1e-4, atol=2e-6)
+    if out.grad is not None:
+        _, used = check_grad(grad_to_f64(out.grad[:, :case.w.V]), g_ref, bf16, what, scale)
+        # the mixed-sign allowance is the exception, not the rule
+        assert used <= 1e-3 * g_ref.size, (what, used)

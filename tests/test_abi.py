@@ -62,7 +62,13 @@ def _args(**kw):
     ({"reduction": L.LMLOSS_REDUCE_SUM, "denominator": 0.0}, L.LMLOSS_ERR_INVALID_ARG),
     ({"reduction": L.LMLOSS_REDUCE_SUM, "denominator": 3.0}, L.LMLOSS_OK),
     ({"teacher_logits": 0x60000, "kl_weight": 0.5}, L.LMLOSS_OK),
-    ({"teacher_logits": 0x60000, "temperature": 2.0}, L.LMLOSS_ERR_UNSUPPORTED),
+    ({"teacher_logits": 0x60000, "temperature": 2.0}, L.LMLOSS_OK),
+    ({"teacher_logits": 0x60000, "temperature": 0.25}, L.LMLOSS_OK),
+    ({"teacher_logits": 0x60000, "temperature": 0.0}, L.LMLOSS_ERR_INVALID_ARG),
+    ({"teacher_logits": 0x60000, "temperature": -1.0}, L.LMLOSS_ERR_INVALID_ARG),
+    ({"teacher_logits": 0x60000, "temperature": float("inf")}, L.LMLOSS_ERR_INVALID_ARG),
+    ({"teacher_logits": 0x60000, "temperature": float("nan")}, L.LMLOSS_ERR_INVALID_ARG),
+    ({"temperature": 0.0}, L.LMLOSS_OK),                                    # ignored without a teacher
     ({"teacher_logits": 0x60004}, L.LMLOSS_ERR_INVALID_ARG),
     ({"segment_ids": 0x70000, "num_segments": 2, "advantages": 0x71000, "old_logprobs": 0x72000}, L.LMLOSS_OK),
     ({"segment_ids": 0x70000, "num_segments": 2, "old_logprobs": 0x72000}, L.LMLOSS_ERR_INVALID_ARG),

@@ -319,15 +319,15 @@ constexpr int kMaxCluster = 16;
 struct ClusterRec {     // one CTA's partial for the current row (32 bytes; 48 with the entropy
                         // or a teacher)
     float m, s;         // CTA max over its non-target columns; sum e^(z - m)
-    float mu, su, w;    // teacher: max, sum e^((u - mu)/tau), cross term (see ma)
+    float mu, su, w;    // teacher: max, sum e^((u - mu)/tau), sum e^((u - mu)/tau) (u - z) over
+                        //   the non-target columns
     float zt;           // target logit (on the CTA that owns the target column)
     int next_row;       // rank 0: row for iteration i + depth (see fused_kernel)
     int next_t;         // rank 0: its target, or -100 when the row is inactive
     float bc;           // sum e^(z - m) (z - m) over the non-target columns (entropy)
     float st;           // tau != 1: sum e^((z - m)/tau) over the non-target columns
-    float ma;           // teacher: max of z over all the CTA's columns, the target's included;
-                        //   w is centred: sum e^((u - mu)/tau) ((u - z) - (mu - ma))
-    float pad2;
+    float sunt;         // teacher: su without the target column (w leaves it out too)
+    float ut;           // teacher logit at the target (on the owner, 0 elsewhere)
 };
 static_assert(sizeof(ClusterRec) == 48, "record is two or three 16-byte pushes");
 
@@ -402,16 +402,15 @@ __device__ __forceinline__ void sums_plain(uint32_t bz, int nvec, int tid, int v
 }
 
 // The same with the teacher slice (guard-free form: a -inf teacher logit makes
-// w NaN, and the caller then takes w again with sum_w_guarded):
-//   su = sum 2^c, c = u Lt - muL,   w = sum 2^c ((u - z) - cw),
+// w NaN, and the caller then takes w again with sum_w_guarded), the target
+// column left out like the student's:
+//   su = sum 2^c, c = u Lt - muL,   w = sum 2^c (u - z),   et = 2^c of the target,
 // with Lt = log2e, or log2(e) / tau at a temperature (TAU), where the student's
 // non-target sum at the temperature is taken too:  st = sum 2^(z Lt - mLt).
-// cw = mu_w - ma_w centres the cross term: a column holding both the teacher's
-// and the student's maximum adds exactly 0 to it.
 template <class IO, int NT, bool ENT, bool TAU>
 __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float mL,
-                                        float muL, float Lt, float mLt, float cw, float& s_out, float& su_out,
-                                        float& w_out, float& b_out, float& st_out)
+                                        float muL, float Lt, float mLt, float& s_out, float& su_out,
+                                        float& w_out, float& b_out, float& st_out, float& et_out)
 {
     constexpr int VN = IO::N;
     const uint64_t L2 = f2_pack(kLog2e, kLog2e);
@@ -419,9 +418,9 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
     const uint64_t nm2 = f2_pack(-mL, -mL);
     const uint64_t nmu2 = f2_pack(-muL, -muL);
     const uint64_t nmt2 = f2_pack(-mLt, -mLt);
-    const uint64_t ncw2 = f2_pack(-cw, -cw);
     const uint64_t neg1 = f2_pack(-1.f, -1.f);
     uint64_t accz = f2_pack(0.f, 0.f), accu = accz, accw = accz, accb = accz, acct = accz;
+    float et = 0.f;
     // one vector: the student terms of every column but lane `kill` (the
     // target's, or -1), the teacher terms of every column
     auto vec = [&](int v, int kill) {
@@ -448,9 +447,12 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
                 if (2 * k + 1 == kill) f1 = 0.f;
                 acct = f2_add(acct, f2_pack(f0, f1));
             }
-            const uint64_t eu = f2_pack(ex2(u0), ex2(u1));
+            float g0 = ex2(u0), g1 = ex2(u1);
+            if (2 * k == kill) { et = g0; g0 = 0.f; }
+            if (2 * k + 1 == kill) { et = g1; g1 = 0.f; }
+            const uint64_t eu = f2_pack(g0, g1);
             accu = f2_add(accu, eu);
-            accw = f2_fma(eu, f2_add(f2_fma(xz, neg1, xu), ncw2), accw);   // e^((u-mu)/tau) ((u - z) - cw)
+            accw = f2_fma(eu, f2_fma(xz, neg1, xu), accw);   // e^((u-mu)/tau) (u - z)
         }
     };
     // the target's vector is taken out of the loop, so the loop body needs no
@@ -468,6 +470,7 @@ __device__ __forceinline__ void sums_kl(uint32_t bz, uint32_t bu, int nvec, int 
     w_out = h0 + h1;
     f2_unpack(acct, h0, h1);
     st_out = TAU ? h0 + h1 : 0.f;
+    et_out = et;
     float b0 = 0.f;
     if (ENT) {
         f2_unpack(accb, h0, h1);
@@ -495,11 +498,11 @@ __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int
     return b;
 }
 
-// w = sum 2^c ((u - z) - cw), c = u Lt - muL, over this thread's columns of
-// the interior (the target's included), skipping 2^c = 0.
+// w = sum 2^c (u - z), c = u Lt - muL, over this thread's non-target columns
+// of the interior, skipping 2^c = 0.
 template <class IO, int NT>
-__device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, int tid, float muL, float Lt,
-                                            float cw)
+__device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, int tid, int vt, int kt, float muL,
+                                            float Lt)
 {
     constexpr int VN = IO::N;
     float w = 0.f;
@@ -509,7 +512,7 @@ __device__ __noinline__ float sum_w_guarded(uint32_t bz, uint32_t bu, int nvec, 
         IO::unpack(lds128(bu + v * 16), y);
         for (int j = 0; j < VN; ++j) {
             const float eu = ex2(fmaf(y[j], Lt, -muL));
-            if (eu > 0.f) w = fmaf(eu, (y[j] - x[j]) - cw, w);
+            if (eu > 0.f && (v != vt || j != kt)) w = fmaf(eu, y[j] - x[j], w);
         }
     }
     return w;
@@ -681,13 +684,12 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         // warp takes its sums against its own maxima and the warps' partials are
         // rebased once, when the CTA's record is built, so no CTA barrier sits
         // between the two passes
-        // With a teacher, also the warp's maximum of z over all its columns (target
-        // included), ma_w: the cross term of the KL is centred on (mu_w, ma_w).
-        float m_w = -INFINITY, mu_w = -INFINITY, ma_w = -INFINITY;
+        // (the thread holding the target column also records the target's logit,
+        // and with a teacher the teacher's, for the merge)
+        float m_w = -INFINITY, mu_w = -INFINITY;
         if (act && mode != kModeGrad) {
             uint32_t accz = IO::max_init(), accu = IO::max_init();
             float mx = -INFINITY, mu = -INFINITY;
-            float ztr = -INFINITY;   // the target logit, on the thread that holds it
 #pragma unroll 4
             for (int v = tid; v < nvec; v += NT) {
                 const uint4 q = lds128(bz + v * 16);
@@ -697,7 +699,14 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 #pragma unroll
                     for (int j = 0; j < VN; ++j) {
                         if (j != kt) mx = fmaxf(mx, x[j]);
-                        else { slot[0] = x[j]; ztr = x[j]; }
+                        else slot[0] = x[j];
+                    }
+                    if (KL) {
+                        float y[VN];
+                        IO::unpack(lds128(bu + v * 16), y);
+#pragma unroll
+                        for (int j = 0; j < VN; ++j)
+                            if (j == kt) slot[1] = y[j];
                     }
                 } else {
                     accz = IO::max_acc(accz, q);
@@ -713,10 +722,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     for (int64_t j = lo; j < hi; ++j) {
                         const float x = IO::load1(p.logits, r * p.ld + j);
                         if (j != t) mx = fmaxf(mx, x);
-                        else { slot[0] = x; ztr = x; }
+                        else slot[0] = x;
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             mu = fmaxf(mu, y);
+                            if (j == t) slot[1] = y;
                         }
                     }
                 }
@@ -728,11 +738,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 mu = fmaxf(mu, IO::max_final(accu));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) mu = fmaxf(mu, __shfl_xor_sync(0xffffffffu, mu, off));
-                // the thread holding the target: vt's thread, or the edge thread
-                // when the target lies in a head or tail column of this slice
-                const int hold = (vt >= 0) ? vt % NT : (owner ? NT - 1 : -1);
-                const float zh = __shfl_sync(0xffffffffu, ztr, hold & 31);
-                ma_w = (hold >= 0 && (hold >> 5) == warp) ? fmaxf(m, zh) : m;
             }
             m_w = m;
             if (KL) mu_w = mu;
@@ -743,20 +748,19 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const float mL = (m_w == -INFINITY) ? 0.f : m_w * kLog2e;
             const float muL = (mu_w == -INFINITY) ? 0.f : mu_w * Lt;
             const float mLt = (!TAU || m_w == -INFINITY) ? 0.f : m_w * Lt;
-            const float cw = (mu_w == -INFINITY || ma_w == -INFINITY) ? 0.f : mu_w - ma_w;
-            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f, st = 0.f;
+            float s0 = 0.f, s1 = 0.f, su = 0.f, w = 0.f, b0 = 0.f, st = 0.f, et = 0.f;
             if (!KL) {
                 if (p.entropy_out) sums_plain<IO, NT, true>(bz, nvec, tid, vt, kt, mL, s0, b0);
                 else sums_plain<IO, NT, false>(bz, nvec, tid, vt, kt, mL, s0, b0);
             }
             if (KL) {
                 if (p.entropy_out)
-                    sums_kl<IO, NT, true, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, cw, s0, su, w, b0, st);
+                    sums_kl<IO, NT, true, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, s0, su, w, b0, st, et);
                 else
-                    sums_kl<IO, NT, false, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, cw, s0, su, w, b0, st);
+                    sums_kl<IO, NT, false, TAU>(bz, bu, nvec, tid, vt, kt, mL, muL, Lt, mLt, s0, su, w, b0, st, et);
                 // a -inf teacher logit gives 0 * -inf = NaN in the guard-free cross
                 // term: a thread that met one takes that sum again with the guard
-                if (isnan(w) && !isnan(su)) w = sum_w_guarded<IO, NT>(bz, bu, nvec, tid, muL, Lt, cw);
+                if (isnan(w) && !isnan(su)) w = sum_w_guarded<IO, NT>(bz, bu, nvec, tid, vt, kt, muL, Lt);
             }
             float s = s0 + s1;
             if (tid == NT - 1) {
@@ -774,18 +778,26 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         if (KL) {
                             const float y = IO::load1(p.teacher, r * p.ld + j);
                             const float eu = ex2(fmaf(y, Lt, -muL));
-                            su += eu;
-                            w += (eu > 0.f) ? eu * ((y - x) - cw) : 0.f;
+                            if (j != t) {
+                                su += eu;
+                                w += (eu > 0.f) ? eu * (y - x) : 0.f;
+                            } else {
+                                et = eu;
+                            }
                         }
                     }
                 }
             }
+            // the teacher's sum over all columns (sua: the target's term folded back
+            // in, for the gradient) and without the target (su, for the KL)
+            float sua = su + et;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 s += __shfl_xor_sync(0xffffffffu, s, off);
                 b0 += __shfl_xor_sync(0xffffffffu, b0, off);
                 if (KL) {
                     su += __shfl_xor_sync(0xffffffffu, su, off);
+                    sua += __shfl_xor_sync(0xffffffffu, sua, off);
                     w += __shfl_xor_sync(0xffffffffu, w, off);
                 }
                 if (TAU) st += __shfl_xor_sync(0xffffffffu, st, off);
@@ -794,7 +806,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 wred[warp] = m_w;
                 wred[64 + warp] = s;
                 wred[192 + warp] = b0;
-                if (KL) { wred[32 + warp] = mu_w; wred[96 + warp] = su; wred[128 + warp] = w; wred[224 + warp] = ma_w; }
+                if (KL) { wred[32 + warp] = mu_w; wred[96 + warp] = sua; wred[128 + warp] = w; wred[224 + warp] = su; }
                 if (TAU) wred[160 + warp] = st;
             }
         }
@@ -810,8 +822,8 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 
         // ---- publish this CTA's record
         if (warp == 0) {
-            float s = 0.f, su = 0.f, w = 0.f, bc = 0.f, st = 0.f;
-            float m_cta = -INFINITY, mu_cta = -INFINITY, ma_cta = -INFINITY;
+            float s = 0.f, su = 0.f, sun = 0.f, w = 0.f, bc = 0.f, st = 0.f;
+            float m_cta = -INFINITY, mu_cta = -INFINITY;
             if (act) {
                 // warp w's sums are against round(m_w log2e): rebase them onto
                 // round(m_cta log2e) (entropy partial: e (a + d) summed = f (b + s d))
@@ -840,23 +852,15 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
 #pragma unroll
                     for (int off = kPubOff; off > 0; off >>= 1)
                         mu_cta = fmaxf(mu_cta, __shfl_xor_sync(0xffffffffu, mu_cta, off));
-                    const float maw = (lane < NW) ? wred[224 + lane] : -INFINITY;
-                    ma_cta = maw;
-#pragma unroll
-                    for (int off = kPubOff; off > 0; off >>= 1)
-                        ma_cta = fmaxf(ma_cta, __shfl_xor_sync(0xffffffffu, ma_cta, off));
                     const float muLc = (mu_cta == -INFINITY) ? 0.f : mu_cta * Lt;
                     const float muLw = (muw == -INFINITY) ? 0.f : muw * Lt;
                     su = (lane < NW) ? wred[96 + lane] : 0.f;
+                    sun = (lane < NW) ? wred[224 + lane] : 0.f;
                     w = (lane < NW) ? wred[128 + lane] : 0.f;
                     const float fu = (su == 0.f) ? 0.f : ex2(muLw - muLc);
-                    // re-centre the cross term from (mu_w, ma_w) onto (mu_cta, ma_cta):
-                    // w + su ((mu_w - ma_w) - (mu_cta - ma_cta)), whose correction is
-                    // exactly 0 for the warp that holds both maxima
-                    const float cwv = (muw == -INFINITY || maw == -INFINITY) ? 0.f : muw - maw;
-                    const float cc = (mu_cta == -INFINITY || ma_cta == -INFINITY) ? 0.f : mu_cta - ma_cta;
-                    w = (su == 0.f) ? 0.f : fu * fmaf(su, cwv - cc, w);
                     su *= fu;
+                    sun *= fu;
+                    w *= fu;
                 }
 #pragma unroll
                 for (int off = kPubOff; off > 0; off >>= 1) {
@@ -864,6 +868,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     bc += __shfl_xor_sync(0xffffffffu, bc, off);
                     if (KL) {
                         su += __shfl_xor_sync(0xffffffffu, su, off);
+                        sun += __shfl_xor_sync(0xffffffffu, sun, off);
                         w += __shfl_xor_sync(0xffffffffu, w, off);
                     }
                     if (TAU) st += __shfl_xor_sync(0xffffffffu, st, off);
@@ -890,20 +895,20 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const float mLt = (m_cta == -INFINITY) ? 0.f : m_cta * Lt;
                 R.st = st * ((m_cta == -INFINITY) ? 1.f : ex2(-fmaf(m_cta, Lt, -mLt)));
             }
-            R.ma = ma_cta;
-            R.pad2 = 0.f;
             R.mu = mu_cta;
             const float fu = (mu_cta == -INFINITY) ? 1.f : ex2(-fmaf(mu_cta, Lt, -muL));
             R.su = su * fu;
+            R.sunt = sun * fu;
             R.w = w * fu;
             R.zt = owner ? slot[0] : 0.f;   // exactly 0 in every CTA but the target's owner
+            R.ut = (KL && owner) ? slot[1] : 0.f;
             R.next_row = (rank == 0) ? claim_b : 0;
             R.next_t = (rank == 0) ? next_t_b : -100;
             const uint4* Rv = reinterpret_cast<const uint4*>(&R);
             const uint32_t my_slot = smem_addr(&rec[(i & 1) * kMaxCluster + rank]);
             const uint32_t my_bar = smem_addr(&rbar[i & 1]);
-            // the third 16 bytes (entropy partial; with a teacher the all-column
-            // maximum and the tempered sum) travel only when used
+            // the third 16 bytes (entropy partial; with a teacher the target's
+            // terms and the tempered sum) travel only when used
             const bool ent = KL || p.entropy_out != nullptr;
             const uint32_t rec_bytes = ent ? 48u : 32u;
             if (lane == 0) mbar_arrive_expect_tx(my_bar, static_cast<uint32_t>(C) * rec_bytes);
@@ -925,7 +930,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             }
             ClusterRec q;
             q.m = -INFINITY; q.s = 0.f; q.mu = -INFINITY; q.su = 0.f; q.w = 0.f; q.zt = 0.f;
-            q.next_row = 0; q.next_t = -100; q.bc = 0.f; q.st = 0.f; q.ma = -INFINITY;
+            q.next_row = 0; q.next_t = -100; q.bc = 0.f; q.st = 0.f; q.sunt = 0.f; q.ut = 0.f;
             if (lane < C) q = rec[(i & 1) * kMaxCluster + lane];
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
@@ -967,20 +972,16 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 const bool ent = p.entropy_out != nullptr;
                 float Bc = (!ent || q.s == 0.f) ? 0.f : fz * (q.bc + q.s * (q.m - M));
                 float Zt = q.zt;   // summed below: every record but the owner's holds exactly 0
-                float Mu = q.mu, Su = 0.f, W = 0.f, Ma = q.ma;
+                float Mu = q.mu, Su = 0.f, Sun = 0.f, W = 0.f;
+                float Ut = q.ut;   // summed like Zt
                 float St = TAU ? q.st * rescale(q.m, M, Lt) : 0.f;
                 if (KL) {
 #pragma unroll
-                    for (int off = kRecOff; off > 0; off >>= 1) {
-                        Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
-                        Ma = fmaxf(Ma, __shfl_xor_sync(0xffffffffu, Ma, off));
-                    }
+                    for (int off = kRecOff; off > 0; off >>= 1) Mu = fmaxf(Mu, __shfl_xor_sync(0xffffffffu, Mu, off));
                     const float f = rescale(q.mu, Mu, Lt);
                     Su = q.su * f;
-                    // the cross term re-centred on the row's (Mu, Ma), as for the CTA's record
-                    const float cr = (q.mu == -INFINITY || q.ma == -INFINITY) ? 0.f : q.mu - q.ma;
-                    const float cM = (Mu == -INFINITY || Ma == -INFINITY) ? 0.f : Mu - Ma;
-                    W = (q.su == 0.f) ? 0.f : f * fmaf(q.su, cr - cM, q.w);
+                    Sun = q.sunt * f;
+                    W = q.w * f;
                 }
 #pragma unroll
                 for (int off = kRecOff; off > 0; off >>= 1) {
@@ -989,7 +990,9 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     Zt += __shfl_xor_sync(0xffffffffu, Zt, off);
                     if (KL) {
                         Su += __shfl_xor_sync(0xffffffffu, Su, off);
+                        Sun += __shfl_xor_sync(0xffffffffu, Sun, off);
                         W += __shfl_xor_sync(0xffffffffu, W, off);
+                        Ut += __shfl_xor_sync(0xffffffffu, Ut, off);
                     }
                     if (TAU) St += __shfl_xor_sync(0xffffffffu, St, off);
                 }
@@ -1014,20 +1017,36 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const float tg = (pt < 0.25f) ? pt - 1.0f : -pnt;
                     // KL = sum q (log q - log p^tau) with log q_j = (u_j - Mu)/tau - ln Su
                     // and log p^tau_j = (z_j - Ma)/tau - (lse_tau - Ma/tau), Ma = max(M, z_t):
-                    //   KL = E_q[(u - Mu) - (z - Ma)] / tau - ln Su + (lse_tau - Ma/tau),
-                    // with the cross term W / Su = E_q[(u - Mu) - (z - Ma)] centred so
-                    // that the column holding both maxima adds exactly 0, and
-                    // lse_tau - Ma/tau = softplus(dT) when z_t >= M, rb otherwise (below):
-                    // no term grows with the logits' offset, so a small KL (both
-                    // distributions confident on one column) keeps its digits.
+                    //   KL = E_q[(u - Mu) - (z - Ma)] / tau - ln Su + (lse_tau - Ma/tau).
+                    // W and Sun leave the target column out, so with c = Mu - Ma
+                    //   Su E_q[(u - Mu) - (z - Ma)] = (W - c Sun) + e_t ((u_t - z_t) - c),
+                    // e_t = e^((u_t - Mu)/tau): the target's part is exactly 0 when teacher
+                    // and student both have their maximum there, and then
+                    // ln Su = (u_t - Mu)/tau + log1p(Sun / e_t) keeps full precision;
+                    // lse_tau - Ma/tau = softplus(dT) when z_t >= M, rb otherwise (below;
+                    // at tau = 1 the NLL, or ln S + softplus(-d)).  No term grows with the
+                    // logits' offset, so a small KL (both confident on the target) keeps
+                    // its digits.
                     float kl = 0.f;
                     // tau != 1: the tempered student p^tau = softmax(z / tau) has
                     //   lse_tau = logaddexp(z_t / tau, M / tau + ln St) = mr / tau + rb
                     // with the reference point mr = M (z_t when no other column is
                     // finite) and, as for the cross-entropy, dT = (M - z_t) / tau + ln St,
                     // rb = ln St + softplus(-dT), p^tau_t = sigmoid(-dT)
-                    float mr = 0.f, rb = 0.f, ptt = 0.f, lnSu = 0.f;
-                    if (KL) lnSu = logf(Su);
+                    // ln Su twice: precisely for the KL (a small KL is a difference of such
+                    // logarithms), by the fast intrinsic for the teacher's gradient offset,
+                    // which sits on the chain to pass C and needs no more than 1e-6
+                    float mr = 0.f, rb = 0.f, ptt = 0.f, lnSu = 0.f, lnSu_g = 0.f, Wc = 0.f;
+                    if (KL) {
+                        lnSu_g = __logf(Su);
+                        const float kappa = TAU ? p.tau_inv : 1.f;
+                        const float Ma = fmaxf(M, zt);
+                        const float c = (Mu == -INFINITY || Ma == -INFINITY) ? 0.f : Mu - Ma;
+                        const float du = Ut - Mu;
+                        const float et = ex2(du * Lt);
+                        Wc = fmaf(-c, Sun, W) + ((et > 0.f) ? et * ((Ut - zt) - c) : 0.f);
+                        lnSu = (et >= 0.5f) ? fmaf(du, kappa, log1pf(__fdividef(Sun, et))) : logf(Su);
+                    }
                     if (TAU) {
                         const float lnSt = (St == 0.f) ? -INFINITY : logf(St);
                         const float dT = fmaf(p.tau_inv, M - zt, lnSt);
@@ -1040,11 +1059,11 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         rb = (St == 0.f) ? 0.f : lnSt + (fmaxf(-dT, 0.f) + l1p);
                         if (isnan(dT)) rb = dT;
                         const float lseMa = (St == 0.f || zt >= M) ? fmaxf(dT, 0.f) + l1p : rb;
-                        kl = fmaf(__fdividef(W, Su), p.tau_inv, lseMa - lnSu);
+                        kl = fmaf(__fdividef(Wc, Su), p.tau_inv, lseMa - lnSu);
                     } else if (KL) {
                         // lse - Ma: NLL when the target is the maximum, else ln S + softplus(-d)
                         const float lseMa = (S == 0.f || zt >= M) ? nll : lnS + sp_neg;
-                        kl = __fdividef(W, Su) + (lseMa - lnSu);
+                        kl = __fdividef(Wc, Su) + (lseMa - lnSu);
                     }
                     const float s = s_tok;
                     const float zc = 2.f * p.alpha * lse;
@@ -1073,16 +1092,16 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     if (TAU) {
                         // b p^tau_j = 2^((z_j - mr) Lt - ct), b q_j = 2^((u_j - Mu) Lt - cq): the
                         // exponent offsets stay small, and the products with log2 e exact
-                        const float rbL = rb * kLog2e, raL = lnSu * kLog2e;
+                        const float rbL = rb * kLog2e, raL = lnSu_g * kLog2e;
                         cf.ltL = rbL;
                         cf.luL = raL;
                         cf.ct = (b_kl > 0.f) ? rbL + (fmaf(rb, kLog2e, -rbL) - log2_b) : INFINITY;
-                        cf.cq = (b_kl > 0.f) ? raL + (fmaf(lnSu, kLog2e, -raL) - log2_b) : INFINITY;
+                        cf.cq = (b_kl > 0.f) ? raL + (fmaf(lnSu_g, kLog2e, -raL) - log2_b) : INFINITY;
                         cf.mr = mr;
                         cf.mu = Mu;
                         cf.gt = (s * p.w_ce + c_r) * tg + s * zc * pt + b_kl * ptt;
                     } else {
-                        const float lu = Mu + lnSu;   // teacher's logsumexp
+                        const float lu = Mu + lnSu_g;   // teacher's logsumexp
                         const float luL = lu * kLog2e;
                         cf.luL = luL;
                         cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;

@@ -114,11 +114,11 @@ def test_tau_forward_only(dev, handle, tau):
     torch.cuda.synchronize()
     assert handle.device_error() == 0
     compare_all(case, out, R, None, f"forward only, tau {tau}")
-    # the fused call agrees: it runs more threads per CTA, so its partial sums are
-    # added in another order, and the KL (a sum of terms of about ln V) may move
-    # by an ulp of those terms
+    # the fused call agrees to the oracle's tolerance: it runs more threads per
+    # CTA, so its partial sums are added in another order, and the KL (formed from
+    # terms of about ln V) may move by a few ulps of those terms
     _, full = run(handle, case, inp=inp)
-    np.testing.assert_allclose(full.kl.cpu().numpy(), out.kl.cpu().numpy(), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(full.kl.cpu().numpy(), out.kl.cpu().numpy(), rtol=1e-4, atol=2e-6)
     np.testing.assert_allclose(full.loss.cpu().numpy(), out.loss.cpu().numpy(), rtol=1e-5)
 
 

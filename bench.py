@@ -75,6 +75,8 @@ def parse():
     ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--nbuf", type=int, default=0)
     ap.add_argument("--rows", type=int, default=0, help="profiling only: fewer rows than the workload")
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="distillation temperature for a workload with a teacher (0: the workload's own)")
     return ap.parse_args()
 
 
@@ -266,9 +268,18 @@ def call_kwargs(w, world, n_active_global):
     return kw
 
 
+def with_temperature(w, args):
+    """The workload at the temperature asked for on the command line (teacher workloads only)."""
+    if args.temperature > 0.0 and w.teacher_sigma is not None:
+        from dataclasses import replace
+        return replace(w, temperature=float(args.temperature))
+    return w
+
+
 def config_of(w, kw, world, grad_mode, restore):
+    extra = {"temperature": w.temperature} if w.teacher_sigma is not None else {}
     return {
-        "workload": w.name, "T_per_gpu": w.T, "V": w.V, "logits": w.dtype,
+        "workload": w.name, "T_per_gpu": w.T, "V": w.V, "logits": w.dtype, **extra,
         "reduction": kw["reduction"], "grad": grad_mode,
         "l2": (f"inputs larger than L2 ({w.T * w.V * w.elem_bytes / 1e9:.2f} GB of logits per step) "
                f"and a {L2_FLUSH_BYTES >> 20} MB L2 flush between steps"),
@@ -321,7 +332,7 @@ def run_reference(args):
         return
     import workloads
 
-    w = workloads.get(args.workload)
+    w = with_temperature(workloads.get(args.workload), args)
     prob = RankSlice(w, 0, 1)
     per_step = []
     rows = 0
@@ -358,6 +369,8 @@ def time_workload(args, name, dev, world, rank, main: bool):
     wl = workloads.get(name)
     if args.rows and main:
         wl = wl.with_shape(args.rows, wl.V)
+    if main:
+        wl = with_temperature(wl, args)
     e2e_on = main and not args.no_e2e
     prob = Problem(wl, dev, rank, world, keep_host=e2e_on)
     w = prob.w
@@ -447,7 +460,8 @@ def time_workload(args, name, dev, world, rank, main: bool):
     value = world * elems_rank / (step_ms / 1e3)
     alg_bytes = w.algorithmic_bytes()
     peak, peak_kind = read_peaks()
-    traffic = read_traffic(w.name, w.T)
+    # a distillation temperature other than 1 runs its own kernel instantiation: its own record
+    traffic = read_traffic(w.name if w.temperature == 1.0 else f"{w.name}@tau={w.temperature:g}", w.T)
     achieved = alg_bytes / (kern_ms / 1e3) / 1e9
 
     # ---- end to end through the C ABI with host buffers

@@ -181,9 +181,9 @@ lmloss_status lmloss_get_device_error(lmloss_handle handle);
 const char* lmloss_status_string(lmloss_status status);
 
 /* Override the fused kernel's launch shape: cluster size (1..16), threads per
- * CTA (128, 256, 384, 512 or 1024) and rows staged per CTA (1 or 2).  0 keeps
- * the automatic choice.  Shapes that do not fit are rejected at the next call
- * with LMLOSS_ERR_UNSUPPORTED. */
+ * CTA (128, 256, 512 or 1024) and rows staged per CTA (1 or 2); other values are
+ * LMLOSS_ERR_INVALID_ARG, and 0 keeps the automatic choice.  Shapes that do not
+ * fit are rejected at the next call with LMLOSS_ERR_UNSUPPORTED. */
 lmloss_status lmloss_set_launch_config(lmloss_handle handle, int cluster, int threads, int nbuf);
 
 /* When enabled (which also resets the record), each call records a pair of

@@ -215,6 +215,15 @@ def test_launch_shapes(dev, handle, cluster, threads, nbuf):
         handle.set_launch_config(0, 0, 0)
 
 
+def test_launch_config_rejects_unbuilt_shapes(dev, handle):
+    """Only the block sizes the library is built for are accepted."""
+    from lm_head_vocab_gb300.lmloss import LMLossError
+    for cluster, threads, nbuf in [(0, 384, 0), (0, 64, 0), (17, 0, 0), (0, 0, 3), (-1, 0, 0)]:
+        with pytest.raises(LMLossError):
+            handle.set_launch_config(cluster, threads, nbuf)
+    handle.set_launch_config(0, 0, 0)
+
+
 @pytest.mark.parametrize("name,shape", [("ce_z_kl_bf16", dict(T=1024, V=30000)),
                                         ("ce_z_bf16", dict(T=2048, V=32000)),
                                         ("confident_bf16", dict(T=2048, V=8000))])

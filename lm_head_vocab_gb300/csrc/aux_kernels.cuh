@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
     __shared__ double part[4][8];
     __shared__ long long npart[8];
     __shared__ double fin[4][kRedBlocks];
-    __shared__ long long nfin[kRedBlocks];
+    __shared__ long long nfin[kRedBlocks];   // one per warp of the last block's tree
     __shared__ bool last;
     // may be launched while the staged-row kernel before it still runs: its
     // per-row results must be complete and visible before any is read
@@ -280,33 +280,39 @@ __global__ void __launch_bounds__(256) reduce_kernel(const CallParams p)
     }
     __syncthreads();
     if (!last) return;
-    // the last block: the block partials are loaded in parallel, then one
-    // thread adds them in block order (the same order on every call)
+    // the last block: the block partials are loaded in parallel and added by
+    // the same fixed-shape shuffle tree (counts with them), then one thread adds
+    // the two warps' sums: the same order on every call
     __threadfence();
     if (tid < kRedBlocks) {
         double v0 = 0.0, v1 = 0.0, v2 = 0.0, v3 = 0.0;
+        long long c = 0;
         if (tid < nb) {
             const volatile double* rp = p.ws.red_part + 4 * tid;
             v0 = rp[0]; v1 = rp[1]; v2 = rp[2]; v3 = rp[3];
-            nfin[tid] = *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[tid]);
+            c = *reinterpret_cast<volatile long long*>(&p.ws.cnt_part[tid]);
         }
         for (int off = 16; off > 0; off >>= 1) {
             v0 += __shfl_xor_sync(0xffffffffu, v0, off);
             v1 += __shfl_xor_sync(0xffffffffu, v1, off);
             v2 += __shfl_xor_sync(0xffffffffu, v2, off);
             v3 += __shfl_xor_sync(0xffffffffu, v3, off);
+            c += __shfl_xor_sync(0xffffffffu, c, off);
         }
-        if (lane == 0) { fin[0][warp] = v0; fin[1][warp] = v1; fin[2][warp] = v2; fin[3][warp] = v3; }
+        if (lane == 0) {
+            fin[0][warp] = v0; fin[1][warp] = v1; fin[2][warp] = v2; fin[3][warp] = v3;
+            nfin[warp] = c;
+        }
     }
     __syncthreads();
     if (tid == 0) {
         double sa = 0.0, sb = 0.0, sc = 0.0, sd = 0.0;
+        long long n = 0;
         for (int k = 0; k < kRedBlocks / 32; ++k) {
             sa += fin[0][k]; sb += fin[1][k]; sc += fin[2][k]; sd += fin[3][k];
+            n += nfin[k];
         }
         p.ws.done[1] = 0u;
-        long long n = 0;
-        for (int k = 0; k < nb; ++k) n += nfin[k];
         const double s = (p.reduction == 1) ? (n > 0 ? 1.0 / static_cast<double>(n) : 0.0) : p.inv_denominator;
         const double ce = s * sa;
         const double z = s * static_cast<double>(p.alpha) * sb;

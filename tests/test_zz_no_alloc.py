@@ -22,10 +22,11 @@ from tests.gpu_util import Case
 pytestmark = pytest.mark.gpu
 
 WANT = ("logp", "lse", "kl", "count", "seg")
-CASES = [
-    ("ce_z_bf16", dict(T=256, V=32000)),
-    ("gspo_z_bf16", dict(T=512, V=8192, packed_len=128)),
-    ("ce_z_kl_bf16", dict(T=64, V=20000)),
+CASES = [   # workload, shape, distillation temperature
+    ("ce_z_bf16", dict(T=256, V=32000), 1.0),
+    ("gspo_z_bf16", dict(T=512, V=8192, packed_len=128), 1.0),
+    ("ce_z_kl_bf16", dict(T=64, V=20000), 1.0),
+    ("ce_z_kl_bf16", dict(T=64, V=20000), 2.0),
 ]
 
 
@@ -74,10 +75,11 @@ def _same(out, ref, gspo):
         assert torch.equal(out.seg_ratio, ref.seg_ratio)
 
 
-@pytest.mark.parametrize("name,shape", CASES, ids=[c[0] for c in CASES])
-def test_noalloc_matches_regular_twice(dev, name, shape):
+@pytest.mark.parametrize("name,shape,tau", CASES, ids=[f"{c[0]}-tau{c[2]:g}" for c in CASES])
+def test_noalloc_matches_regular_twice(dev, name, shape, tau):
+    from dataclasses import replace
     from lm_head_vocab_gb300 import LMLoss
-    case = Case(workloads.get(name).with_shape(**shape), dev)
+    case = Case(replace(workloads.get(name).with_shape(**shape), temperature=tau), dev)
     inp = case.device_inputs()
     h = LMLoss(0, max_T=case.w.T, max_segments=max(1, case.S))
     try:

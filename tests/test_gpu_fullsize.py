@@ -9,10 +9,11 @@ then checks what it can compute one row at a time:
     gradient < 0, the row summing to ~0) from the per-row outputs;
   * gspo_z_bf16 (32768 x 151936): the full seam (segment counts and flags
     bit-exact), the losses, and sampled rows' gradients;
-  * ce_z_kl_bf16 (65536 x 262144, student and teacher 34 GB each): every row's
-    statistics (log-prob, lse, KL) and the five losses against the oracle, run
-    on each chunk of rows as it is generated (the host never holds the whole
-    68 GB), and sampled rows' gradients.
+  * ce_z_kl_bf16 (65536 x 262144, student and teacher 34 GB each), at the
+    workload's temperature 1 and at 2: every row's statistics (log-prob, lse,
+    KL) and the five losses against the oracle, run on each chunk of rows as it
+    is generated (the host never holds the whole 68 GB), and sampled rows'
+    gradients.
 Tolerances are the same as in test_gpu_parity.py.
 """
 import numpy as np
@@ -199,8 +200,11 @@ def test_gspo_z_bf16_full(dev):
     check_rows(out, w, rows, Rs, g, gs)
 
 
-def test_ce_z_kl_bf16_full(dev):
-    w = workloads.get("ce_z_kl_bf16")
+@pytest.mark.parametrize("tau", [1.0, 2.0])
+def test_ce_z_kl_bf16_full(dev, tau):
+    """At the workload's own temperature 1, and at 2 (the other instantiation)."""
+    from dataclasses import replace
+    w = replace(workloads.get("ce_z_kl_bf16"), temperature=tau)
     tg, mk = w.targets(), w.loss_mask()
     nll, lse, kl = (np.zeros(w.T) for _ in range(3))
     act = oracle.active_mask(tg, mk).astype(bool)

@@ -122,6 +122,15 @@ class Problem:
     reduction: int = REDUCE_TOKEN_MEAN
     denominator: float = 1.0
 
+    def __post_init__(self):
+        # the C oracle reads the buffers by these element types: anything else
+        # would be reinterpreted, not converted
+        if self.logits.dtype not in (np.uint16, np.float32) or self.logits.ndim != 2:
+            raise TypeError("logits must be a 2-D uint16 (bf16 bits) or float32 array")
+        if self.teacher is not None and (self.teacher.dtype != self.logits.dtype
+                                         or self.teacher.shape != self.logits.shape):
+            raise TypeError("teacher must match logits in dtype and shape")
+
     @property
     def T(self) -> int:
         return int(self.logits.shape[0])

@@ -33,6 +33,8 @@ MUTATIONS = [
     ("entropy_max_term_rounds_to_zero", "double nlogp = (j == k) ? l1 :", "double nlogp = (j == k) ? 0.0 :"),
     ("wrong_row_stride", "out[j] = orc_elem(dtype, base, r * ld + j);", "out[j] = orc_elem(dtype, base, r * V + j);"),
     ("bf16_decode_wrong_shift", "[idx] << 16;", "[idx] << 15;"),
+    ("kl_grad_times_tau", "term += w_kl * (p_tau - q) / temperature;", "term += w_kl * (p_tau - q) * temperature;"),
+    ("teacher_not_tempered", "a[j] = u[j] / tau;", "a[j] = u[j];"),
 ]
 
 
@@ -73,6 +75,9 @@ def _pins_pass():
         lambda: pins.test_brute_force_mpmath("kl_tau2", 2, 3, dict(teacher=True, kl_weight=0.7,
                                                                     temperature=2.0, z_alpha=0.01)),
         lambda: pins.test_bf16_inputs_match_fp32_bit_for_bit(),
+        lambda: pins.test_two_class_closed_form_temperature(0.5),
+        lambda: pins.test_torch_fp64_autograd_temperature(3.0),
+        lambda: pins.test_kl_shift_invariance(0.25),
     ]
     # the stride mutation only shows with ld > V
     z = np.random.default_rng(0).normal(size=(3, 8)).astype(np.float32)

@@ -154,6 +154,88 @@ def test_two_class_closed_form(seed):
         np.testing.assert_allclose(g[r], (g_ce + w_kl * g_kl) / T, rtol=1e-11, atol=1e-16)
 
 
+@pytest.mark.parametrize("tau", [0.1, 0.5, 3.0, 10.0])
+def test_two_class_closed_form_temperature(tau):
+    """Distillation at a temperature, two classes: KL(Bern(q) || Bern(p^tau)) with
+    q = sigmoid((u1 - u0)/tau), p^tau = sigmoid((z1 - z0)/tau), and its gradient
+    w_kl (p^tau - q)/tau, no tau^2 factor (the oracle's reading of the pages'
+    distillation term)."""
+    rng = np.random.default_rng(int(tau * 10))
+    T = 6
+    z = rng.normal(0, 2, size=(T, 2)).astype(np.float32)
+    u = rng.normal(0, 2, size=(T, 2)).astype(np.float32)
+    t = rng.integers(0, 2, size=T)
+    w_kl = 0.5
+    P = Problem(logits=z, V=2, targets=t, teacher=u, kl_weight=w_kl, temperature=tau, ce_weight=0.0)
+    R, g = run(P)
+    zd, ud = z.astype(np.float64), u.astype(np.float64)
+    for r in range(T):
+        du, dz = (ud[r, 1] - ud[r, 0]) / tau, (zd[r, 1] - zd[r, 0]) / tau
+        assert R.kl[r] == pytest.approx(bern_kl(du, dz), rel=1e-10, abs=1e-14)
+        p1 = 1.0 / (1.0 + math.exp(-dz))
+        q1 = 1.0 / (1.0 + math.exp(-du))
+        g_kl = np.array([-(p1 - q1), p1 - q1]) / tau
+        np.testing.assert_allclose(g[r], w_kl * g_kl / T, rtol=1e-10, atol=1e-16)
+
+
+@pytest.mark.parametrize("tau", [0.5, 3.0])
+def test_torch_fp64_autograd_temperature(tau):
+    """The same against PyTorch fp64: kl_div of the tempered log-softmaxes, and
+    autograd through z for the gradient."""
+    rng = np.random.default_rng(int(tau * 7))
+    T, V = 12, 301
+    z = rng.normal(0, 3, size=(T, V)).astype(np.float32)
+    u = (z + rng.normal(0, 1, size=(T, V))).astype(np.float32)
+    t = rng.integers(0, V, size=T)
+    t[3] = -100
+    w_kl = 0.5
+    P = Problem(logits=z, V=V, targets=t, teacher=u, kl_weight=w_kl, temperature=tau)
+    R, g = run(P)
+    zt = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    ut = torch.tensor(u, dtype=torch.float64)
+    tt = torch.tensor(t)
+    act = tt != -100
+    N = int(act.sum())
+    ce = torch.nn.functional.cross_entropy(zt, tt, ignore_index=-100, reduction="sum") / N
+    kl = torch.nn.functional.kl_div(torch.log_softmax(zt[act] / tau, 1), torch.log_softmax(ut[act] / tau, 1),
+                                    log_target=True, reduction="sum") / N
+    (ce + w_kl * kl).backward()
+    assert R.kl_loss == pytest.approx(kl.item(), rel=1e-10)
+    np.testing.assert_allclose(g, zt.grad.numpy(), rtol=1e-9, atol=1e-15)
+
+
+def test_problem_rejects_other_dtypes():
+    """The oracle reads float32 or bf16 bits only; a float64 array is refused,
+    not reinterpreted."""
+    z = np.zeros((2, 4))
+    with pytest.raises(TypeError):
+        Problem(logits=z, V=4, targets=np.zeros(2, dtype=np.int64))
+    with pytest.raises(TypeError):
+        Problem(logits=z.astype(np.float32), V=4, targets=np.zeros(2, dtype=np.int64), teacher=z)
+
+
+@pytest.mark.parametrize("tau", [0.25, 1.0, 4.0])
+def test_kl_shift_invariance(tau):
+    """Adding a constant to every teacher logit, or to every student logit, of a
+    row changes neither distribution: the KL and its gradient stay as they were."""
+    rng = np.random.default_rng(17)
+    T, V = 5, 64
+    # values on a 1/64 grid, so the shifted logits are exact in float32 too
+    z = np.round(rng.normal(0, 2, size=(T, V)) * 64) / 64
+    u = z + np.round(rng.normal(0, 1, size=(T, V)) * 64) / 64
+    t = rng.integers(0, V, size=T)
+    f = np.float32
+    base = run(Problem(logits=z.astype(f), V=V, targets=t, teacher=u.astype(f), kl_weight=1.0, ce_weight=0.0,
+                       temperature=tau))
+    for dz, du in [(0.0, 7.5), (-3.25, 0.0), (2.0, -9.0)]:
+        R, g = run(Problem(logits=(z + dz).astype(f), V=V, targets=t, teacher=(u + du).astype(f), kl_weight=1.0,
+                           ce_weight=0.0, temperature=tau))
+        np.testing.assert_allclose(R.kl, base[0].kl, rtol=1e-11, atol=1e-14)
+        # absolute at the terms' scale: where p^tau - q cancels, fp64's rounding of
+        # the shifted exponent arguments (of size ~40 at tau = 1/4) shows at 1e-15
+        np.testing.assert_allclose(g, base[1], rtol=1e-10, atol=1e-14)
+
+
 # --------------------------------------------------------------------------
 # Invariant: CE, KL and GSPO parts of a row gradient sum to 0; z part to 2 a lse s.
 # --------------------------------------------------------------------------

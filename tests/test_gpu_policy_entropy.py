@@ -176,6 +176,47 @@ def test_grpo_parity(dev, handle, reduction):
     check_grad(grad_to_f64(out.grad[torch.from_numpy(np.where(keep)[0]).to(dev)]), g_ref[keep], True, "grpo")
 
 
+@pytest.mark.parametrize("tau", [1.0, 2.0])
+def test_grpo_with_teacher(dev, handle, tau):
+    """The token-level policy term together with distillation (at temperature
+    1 and 2): the policy coefficient of a row joins the cross-entropy's in the
+    gradient, the teacher's term stays as it is."""
+    from dataclasses import replace
+    w = replace(workloads.get("ce_z_kl_bf16").with_shape(T=256, V=30011), temperature=tau)
+    case = Case(w, dev)
+    rng = np.random.default_rng(31)
+    tok_adv = rng.normal(0, 1, size=w.T).astype(np.float32)
+    R0 = oracle.forward(oracle.Problem(logits=case.x, V=w.V, targets=case.targets, loss_mask=case.mask))
+    old = (R0.logp + rng.normal(0.0, 0.25, size=w.T)).astype(np.float32)
+    P = oracle.Problem(logits=case.x, V=w.V, targets=case.targets, loss_mask=case.mask, ce_weight=w.ce_weight,
+                       z_alpha=w.z_alpha, teacher=case.u, kl_weight=w.kl_weight, temperature=w.temperature,
+                       token_advantages=tok_adv, old_logprobs=old, clip_eps_low=0.2, clip_eps_high=0.28)
+    R, g_ref, scale = oracle.forward_backward(P, with_scale=True)
+    inp = case.device_inputs()
+    out = handle.forward_backward(
+        inp["logits"], inp["targets"], inp["loss_mask"], teacher_logits=inp["teacher_logits"],
+        ce_weight=w.ce_weight, z_alpha=w.z_alpha, kl_weight=w.kl_weight, temperature=w.temperature,
+        token_advantages=torch.from_numpy(tok_adv).to(dev), old_logprobs=torch.from_numpy(old).to(dev),
+        clip_eps_low=0.2, clip_eps_high=0.28, grad="new", want=("logp", "lse", "kl", "count"))
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    act = R.active.astype(bool)
+    rho = np.exp(R.logp - old.astype(np.float64))
+    lo, hi = 0.8, 1.28
+    clipped = act & ((rho < lo) | (rho > hi))
+    assert 0.05 * act.sum() < clipped.sum() < 0.8 * act.sum()    # both branches are exercised
+    loss = out.loss.cpu().numpy().astype(np.float64)
+    mag = _policy_mag(P, R)
+    assert abs(loss[4] - R.gspo) <= 1e-5 * mag, (loss[4], R.gspo, mag)
+    assert abs(loss[0] - R.total) <= 1e-5 * (abs(R.total) + mag)
+    assert rel(loss[1], R.ce) <= 1e-5 and rel(loss[2], R.z) <= 1e-5 and rel(loss[3], R.kl_loss) <= 1e-5
+    np.testing.assert_allclose(out.kl.cpu().numpy()[act], R.kl[act], rtol=1e-4, atol=2e-6)
+    amb = act & ((np.abs(rho - lo) < 1e-5 * lo) | (np.abs(rho - hi) < 1e-5 * hi))
+    keep = np.where(~amb)[0]
+    check_grad(grad_to_f64(out.grad[torch.from_numpy(keep).to(dev)]), g_ref[keep], True,
+               f"grpo with teacher, tau {tau}", scale[keep])
+
+
 def test_grpo_forward_only_matches_fused(dev, handle):
     """The policy loss from the statistics-only launch equals the fused one."""
     w = workloads.get("gspo_z_bf16").with_shape(T=512, V=40000, packed_len=128)

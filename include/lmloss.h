@@ -43,7 +43,8 @@ extern "C" {
 typedef enum {
     LMLOSS_OK = 0,
     LMLOSS_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, ld < V, ...        */
-    LMLOSS_ERR_UNSUPPORTED = 2,   /* valid but not implemented (see lmloss_forward_backward) */
+    LMLOSS_ERR_UNSUPPORTED = 2,   /* valid but not served: a launch shape that does not fit, */
+                                  /* T >= 2^30, a shard call with a teacher or policy term    */
     LMLOSS_ERR_CUDA = 3,          /* a CUDA runtime call failed                            */
     LMLOSS_ERR_BAD_TARGET = 4,    /* device: target not in [0, V) and not -100             */
     LMLOSS_ERR_BAD_SEGMENT = 5,   /* device: segment id >= num_segments                    */
@@ -135,7 +136,7 @@ typedef struct {
 } lmloss_call_info;
 
 /* Create a handle on `device`: allocates the workspace for calls with up to
- * max_T rows and max_segments GSPO segments (about 12 B per row plus 40 B per
+ * max_T rows and max_segments GSPO segments (40 B per row plus about 40 B per
  * segment) and the device error word.  The caller owns the handle. */
 lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, int32_t max_segments);
 
@@ -161,7 +162,8 @@ lmloss_status lmloss_check_args(const lmloss_args* args);
  *   - GSPO: statistics pass, segment seam, gradient pass (the seam must see
  *     every row of a segment before any gradient, so the logits are read twice)
  *     [Fast-LLM PR 552, "Approach": GSPO's backward follows its eager seam].
- * Unsupported (LMLOSS_ERR_UNSUPPORTED): teacher together with GSPO.
+ * A teacher combines with every other term, GSPO included (its gradient pass
+ * reads the teacher's row statistics back from the workspace).
  * loss_out is written on every path.  The gradient is
  *   s * (ce_weight (p - onehot) + 2 z_alpha lse p + kl_weight (p^tau - q) / tau)
  *     + c_r (p - onehot)
@@ -213,7 +215,7 @@ lmloss_status lmloss_get_call_info(lmloss_handle handle, lmloss_call_info* info)
  *
  * Same arguments, results and asynchrony as lmloss_forward_backward, on the
  * current device, without a handle.  It allocates nothing: its workspace is a
- * fixed array of about 1.2 MB inside this library, which every GPU that loads
+ * fixed array of about 2.8 MB inside this library, which every GPU that loads
  * the library holds until the process exits.  Limits: T <= LMLOSS_NOALLOC_MAX_T
  * rows and, with GSPO, num_segments <= LMLOSS_NOALLOC_MAX_SEGMENTS; a larger
  * call returns LMLOSS_ERR_INVALID_ARG before anything is launched.

@@ -148,6 +148,9 @@ struct Workspace {
     float* row_lse;      // [max_T]
     float* row_kl;       // [max_T]
     float* row_pol;      // [max_T] per-token GRPO loss
+    float* row_tu;       // [max_T][2] teacher: Mu, ln Su (statistics pass with a teacher, for
+                         //   GSPO's gradient pass)
+    float* row_tt;       // [max_T][4] tau != 1: mr, rb, p^tau_t, 0 (likewise)
     int64_t* n_active;   // [1]
     int64_t* n_nonempty; // [1]
     double* gspo_sum;    // [1]  sum of L_i (unscaled)
@@ -344,6 +347,75 @@ struct RowCoef {        // the row's gradient coefficients, shared by the CTA's 
     // with the reference points mr (student) and mu (teacher)
     float ct, ltL, mr, mu;
 };
+
+// The row's gradient coefficients (see RowCoef) from its scalars: token scale
+// s, lse, the target's CE gradient tg and probability pt, the policy
+// coefficient c_r, and with a teacher its Mu and ln Su, and at a temperature the
+// tempered student's reference point mr, offset rb and target probability ptt.
+// The same arithmetic for the fused pass and for GSPO's gradient pass, which
+// reads these scalars back from the workspace.
+template <bool KL, bool TAU>
+__device__ __forceinline__ RowCoef row_coef(float s, float w_ce, float alpha, float w_kl, float lse, float tg,
+                                            float pt, float c_r, float b_kl, float log2_b, bool a_fixed,
+                                            float log2_a_fixed, float Mu, float lnSu_g, float mr, float rb,
+                                            float ptt)
+{
+    const float zc = 2.f * alpha * lse;
+    const float a = s * (w_ce + zc + (TAU ? 0.f : w_kl)) + c_r;
+    RowCoef cf;
+    // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
+    const float lseL = lse * kLog2e;
+    const float lseL_err = fmaf(lse, kLog2e, -lseL);
+    // (a - a) keeps a NaN coefficient (an infinite lse) a NaN
+    const float log2_a = a_fixed ? log2_a_fixed + (a - a) : __log2f(fabsf(a));
+    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2_a);
+    cf.neg = a < 0.f;
+    cf.lseL = lseL;
+    cf.a = a;
+    cf.b = KL ? b_kl : 0.f;
+    if (TAU) {
+        // b p^tau_j = 2^((z_j - mr) Lt - ct), b q_j = 2^((u_j - Mu) Lt - cq): the
+        // exponent offsets stay small, and the products with log2 e exact
+        const float rbL = rb * kLog2e, raL = lnSu_g * kLog2e;
+        cf.ltL = rbL;
+        cf.luL = raL;
+        cf.ct = (b_kl > 0.f) ? rbL + (fmaf(rb, kLog2e, -rbL) - log2_b) : INFINITY;
+        cf.cq = (b_kl > 0.f) ? raL + (fmaf(lnSu_g, kLog2e, -raL) - log2_b) : INFINITY;
+        cf.mr = mr;
+        cf.mu = Mu;
+        cf.gt = (s * w_ce + c_r) * tg + s * zc * pt + b_kl * ptt;
+    } else if (KL) {
+        const float lu = Mu + lnSu_g;   // teacher's logsumexp
+        const float luL = lu * kLog2e;
+        cf.luL = luL;
+        cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;
+        cf.ct = INFINITY;
+        cf.ltL = 0.f;
+        cf.mr = 0.f;
+        cf.mu = 0.f;
+        cf.gt = (s * w_ce + c_r) * tg + s * (zc + w_kl) * pt;
+    } else {
+        cf.luL = 0.f;
+        cf.cq = INFINITY;
+        cf.ct = INFINITY;
+        cf.ltL = 0.f;
+        cf.mr = 0.f;
+        cf.mu = 0.f;
+        cf.gt = (s * w_ce + c_r) * tg + s * zc * pt;
+    }
+    return cf;
+}
+
+// The same for GSPO's gradient pass, out of line: that pass runs in the same
+// instantiation as the fused one, whose merge this keeps as it was.
+template <bool KL, bool TAU>
+__device__ __noinline__ RowCoef row_coef_grad(float s, float w_ce, float alpha, float w_kl, float lse, float tg,
+                                              float pt, float c_r, float b_kl, float log2_b, float Mu,
+                                              float lnSu_g, float mr, float rb, float ptt)
+{
+    return row_coef<KL, TAU>(s, w_ce, alpha, w_kl, lse, tg, pt, c_r, b_kl, log2_b, false, 0.f, Mu, lnSu_g, mr, rb,
+                             ptt);
+}
 
 template <class IO, int NT>
 __device__ __noinline__ float sum_ea_guarded(uint32_t bz, int nvec, int tid, int vt, int kt, float mL);
@@ -582,7 +654,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
     // at tau = 1 (where p^tau = p), a = s w_ce otherwise.
     const float b_kl = s_tok * p.w_kl * (TAU ? p.tau_inv : 1.f);
     const float log2_b = (b_kl > 0.f) ? log2f(b_kl) : 0.f;
-    const bool a_fixed = p.alpha == 0.f && !p.tok_adv;
+    const bool a_fixed = p.alpha == 0.f && !p.tok_adv;   // (GSPO's gradient pass does not use it)
     const float log2_a_fixed = log2f(fabsf(s_tok * (p.w_ce + (TAU ? 0.f : p.w_kl))));
     // base-2 factor of the teacher's exponentials (and of the student's at the temperature)
     const float Lt = TAU ? p.tau_l2 : kLog2e;
@@ -942,25 +1014,15 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     const float lse = bad ? nll : g_lse;
                     const float pt = expf(-nll);
                     const float tg = (pt < 0.25f) ? pt - 1.0f : expm1f(-nll);
-                    const float s = s_tok;
-                    const float zc = 2.f * p.alpha * lse;
-                    const float a = s * (p.w_ce + zc) + g_cr;
-                    RowCoef cf;
-                    const float lseL = lse * kLog2e;
-                    const float lseL_err = fmaf(lse, kLog2e, -lseL);
-                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - __log2f(fabsf(a)));
-                    cf.neg = a < 0.f;
-                    cf.lseL = lseL;
-                    cf.luL = 0.f;
-                    cf.a = a;
-                    cf.b = 0.f;
-                    cf.cq = INFINITY;
-                    cf.ct = INFINITY;
-                    cf.ltL = 0.f;
-                    cf.mr = 0.f;
-                    cf.mu = 0.f;
-                    cf.gt = (s * p.w_ce + g_cr) * tg + s * zc * pt;
-                    *coef = cf;
+                    // with a teacher, its statistics from the statistics pass (loaded here,
+                    // not with the others above: the fused pass shares this code and
+                    // keeps its registers for the row's sweeps)
+                    float2 g_tu = make_float2(0.f, 0.f);
+                    float4 g_tt = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (KL && !bad) g_tu = reinterpret_cast<const float2*>(p.ws.row_tu)[r];
+                    if (TAU && !bad) g_tt = reinterpret_cast<const float4*>(p.ws.row_tt)[r];
+                    *coef = row_coef_grad<KL, TAU>(s_tok, p.w_ce, p.alpha, p.w_kl, lse, tg, pt, g_cr, b_kl, log2_b,
+                                                   g_tu.x, g_tu.y, g_tt.x, g_tt.y, g_tt.z);
                 }
             } else if (act) {
                 float M = q.m;
@@ -1066,7 +1128,6 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         kl = __fdividef(Wc, Su) + (lseMa - lnSu);
                     }
                     const float s = s_tok;
-                    const float zc = 2.f * p.alpha * lse;
                     // GRPO, token level: rho = exp(logp - old), L = -min(rho A, clamp(rho) A);
                     // when the unclipped branch is taken its gradient is s A rho (p - onehot)
                     float c_r = 0.f, pol = 0.f;
@@ -1077,46 +1138,18 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                         if (rho * g_adv <= rc * g_adv) c_r = s * g_adv * rho;
                         if (isnan(rho) || isnan(g_adv)) { pol = rho + g_adv; c_r = pol; }
                     }
-                    const float a = s * (p.w_ce + zc + (TAU ? 0.f : p.w_kl)) + c_r;
-                    RowCoef cf;
-                    // cz = lse log2e - log2|a|, with the product lse*log2e formed exactly
-                    const float lseL = lse * kLog2e;
-                    const float lseL_err = fmaf(lse, kLog2e, -lseL);
-                    // (a - a) keeps a NaN coefficient (an infinite lse) a NaN
-                    const float log2_a = a_fixed ? log2_a_fixed + (a - a) : __log2f(fabsf(a));
-                    cf.cz = (a == 0.f) ? INFINITY : lseL + (lseL_err - log2_a);
-                    cf.neg = a < 0.f;
-                    cf.lseL = lseL;
-                    cf.a = a;
-                    cf.b = b_kl;
-                    if (TAU) {
-                        // b p^tau_j = 2^((z_j - mr) Lt - ct), b q_j = 2^((u_j - Mu) Lt - cq): the
-                        // exponent offsets stay small, and the products with log2 e exact
-                        const float rbL = rb * kLog2e, raL = lnSu_g * kLog2e;
-                        cf.ltL = rbL;
-                        cf.luL = raL;
-                        cf.ct = (b_kl > 0.f) ? rbL + (fmaf(rb, kLog2e, -rbL) - log2_b) : INFINITY;
-                        cf.cq = (b_kl > 0.f) ? raL + (fmaf(lnSu_g, kLog2e, -raL) - log2_b) : INFINITY;
-                        cf.mr = mr;
-                        cf.mu = Mu;
-                        cf.gt = (s * p.w_ce + c_r) * tg + s * zc * pt + b_kl * ptt;
-                    } else {
-                        const float lu = Mu + lnSu_g;   // teacher's logsumexp
-                        const float luL = lu * kLog2e;
-                        cf.luL = luL;
-                        cf.cq = (b_kl > 0.f) ? luL + (fmaf(lu, kLog2e, -luL) - log2_b) : INFINITY;
-                        cf.ct = INFINITY;
-                        cf.ltL = 0.f;
-                        cf.mr = 0.f;
-                        cf.mu = 0.f;
-                        cf.gt = (s * p.w_ce + c_r) * tg + s * (zc + p.w_kl) * pt;
-                    }
-                    *coef = cf;
+                    *coef = row_coef<KL, TAU>(s, p.w_ce, p.alpha, p.w_kl, lse, tg, pt, c_r, b_kl, log2_b, a_fixed,
+                                              log2_a_fixed, Mu, lnSu_g, mr, rb, ptt);
                     if (rank == 0) {
                         p.ws.row_nll[r] = nll;
                         p.ws.row_lse[r] = lse;
                         p.ws.row_kl[r] = kl;
                         p.ws.row_pol[r] = pol;
+                        // the teacher's statistics, for GSPO's gradient pass
+                        if (KL && EARLY && p.seg_ids) {
+                            reinterpret_cast<float2*>(p.ws.row_tu)[r] = make_float2(Mu, lnSu_g);
+                            if (TAU) reinterpret_cast<float4*>(p.ws.row_tt)[r] = make_float4(mr, rb, ptt, 0.f);
+                        }
                         if (p.entropy_out) {
                             // H = sum p (-log p): the target gives p_t NLL; a non-target j gives
                             // p_j (lse - z_j) with p_j = p_nt e^(z_j - M) / S and

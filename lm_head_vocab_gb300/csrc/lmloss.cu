@@ -88,7 +88,6 @@ lmloss_status check(const lmloss_args* a, bool need_loss = true)
         if (a->T > 0 && !a->old_logprobs) return LMLOSS_ERR_INVALID_ARG;
         if (a->num_segments > 0 && !a->advantages) return LMLOSS_ERR_INVALID_ARG;
         if (!(a->clip_eps_low >= 0.f) || !(a->clip_eps_high >= 0.f)) return LMLOSS_ERR_INVALID_ARG;
-        if (a->teacher_logits) return LMLOSS_ERR_UNSUPPORTED;
     }
     if (a->token_advantages) {
         if (a->segment_ids) return LMLOSS_ERR_INVALID_ARG;   // one policy term per call
@@ -368,6 +367,7 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     const size_t o_nll = take(4 * T), o_lse = take(4 * T), o_kl = take(4 * T), o_pol = take(4 * T);
+    const size_t o_tu = take(8 * T), o_tt = take(16 * T);
     const size_t o_scal = take(64);
     const size_t o_sn = take(4 * S), o_dq = take(8 * S), o_aq = take(8 * S), o_nf = take(12 * S), o_coef = take(4 * S);
     const size_t o_ctr = take(16);
@@ -382,6 +382,8 @@ lmloss_status lmloss_create(lmloss_handle* handle, int device, int64_t max_T, in
     h->ws.row_lse = reinterpret_cast<float*>(base + o_lse);
     h->ws.row_kl = reinterpret_cast<float*>(base + o_kl);
     h->ws.row_pol = reinterpret_cast<float*>(base + o_pol);
+    h->ws.row_tu = reinterpret_cast<float*>(base + o_tu);
+    h->ws.row_tt = reinterpret_cast<float*>(base + o_tt);
     h->ws.n_active = reinterpret_cast<int64_t*>(base + o_scal);
     h->ws.n_nonempty = reinterpret_cast<int64_t*>(base + o_scal + 8);
     h->ws.gspo_sum = reinterpret_cast<double*>(base + o_scal + 16);
@@ -705,7 +707,9 @@ struct NoAllocLayout {
     static constexpr size_t lse = nll + na_align(4 * kNoAllocMaxT);
     static constexpr size_t kl = lse + na_align(4 * kNoAllocMaxT);
     static constexpr size_t pol = kl + na_align(4 * kNoAllocMaxT);
-    static constexpr size_t scal = pol + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t tu = pol + na_align(4 * kNoAllocMaxT);
+    static constexpr size_t tt = tu + na_align(8 * kNoAllocMaxT);
+    static constexpr size_t scal = tt + na_align(16 * kNoAllocMaxT);
     static constexpr size_t seg_n = scal + na_align(64);
     static constexpr size_t seg_dq = seg_n + na_align(4 * kNoAllocMaxS);
     static constexpr size_t seg_absq = seg_dq + na_align(8 * kNoAllocMaxS);
@@ -794,6 +798,8 @@ extern "C" lmloss_status lmloss_forward_backward_noalloc(const lmloss_args* a, c
     ctx.ws.row_lse = reinterpret_cast<float*>(b + L::lse);
     ctx.ws.row_kl = reinterpret_cast<float*>(b + L::kl);
     ctx.ws.row_pol = reinterpret_cast<float*>(b + L::pol);
+    ctx.ws.row_tu = reinterpret_cast<float*>(b + L::tu);
+    ctx.ws.row_tt = reinterpret_cast<float*>(b + L::tt);
     ctx.ws.n_active = reinterpret_cast<int64_t*>(b + L::scal);
     ctx.ws.n_nonempty = reinterpret_cast<int64_t*>(b + L::scal + 8);
     ctx.ws.gspo_sum = reinterpret_cast<double*>(b + L::scal + 16);

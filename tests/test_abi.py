@@ -76,7 +76,7 @@ def _args(**kw):
     ({"segment_ids": 0x70000, "num_segments": -1, "advantages": 0x71000, "old_logprobs": 0x72000},
      L.LMLOSS_ERR_INVALID_ARG),
     ({"segment_ids": 0x70000, "num_segments": 2, "advantages": 0x71000, "old_logprobs": 0x72000,
-      "teacher_logits": 0x60000}, L.LMLOSS_ERR_UNSUPPORTED),
+      "teacher_logits": 0x60000}, L.LMLOSS_OK),                                   # GSPO with a teacher
     ({"segment_ids": 0x70000, "num_segments": 2, "advantages": 0x71000, "old_logprobs": 0x72000,
       "clip_eps_low": -0.1}, L.LMLOSS_ERR_INVALID_ARG),
 ])

@@ -215,6 +215,28 @@ def test_launch_shapes(dev, handle, cluster, threads, nbuf):
         handle.set_launch_config(0, 0, 0)
 
 
+@pytest.mark.parametrize("tau", [1.0, 2.0])
+def test_gspo_with_teacher(dev, handle, tau):
+    """GSPO together with distillation (and cross-entropy): the statistics pass
+    keeps the teacher's row statistics for the gradient pass that follows the
+    seam.  Every output against the oracle, the seam's counts and flags as in
+    the GSPO parity case."""
+    from dataclasses import replace
+    w = workloads.get("gspo_z_bf16").with_shape(T=1024, V=40000, packed_len=256)
+    w = replace(w, teacher_sigma=1.0, kl_weight=0.5, temperature=tau, ce_weight=0.3)
+    case = Case(w, dev)
+    R, g_ref, scale = oracle.forward_backward(case.P, with_scale=True)
+    inp, out = run(handle, case)
+    compare_all(case, out, R, g_ref, f"gspo with teacher, tau {tau}", scale)
+    assert np.array_equal(out.seg_count.cpu().numpy(), R.seam.n)
+    flag = out.seg_flag.cpu().numpy()
+    ratio = R.seam.ratio
+    lo, hi = 1 - w.clip_eps_low, 1 + w.clip_eps_high
+    amb = (np.abs(ratio - lo) < 1e-6 * lo) | (np.abs(ratio - hi) < 1e-6 * hi)
+    assert np.array_equal(flag[~amb], R.seam.flag[~amb])
+    assert handle.call_info()["path"] == 2
+
+
 def test_launch_config_rejects_unbuilt_shapes(dev, handle):
     """Only the block sizes the library is built for are accepted."""
     from lm_head_vocab_gb300.lmloss import LMLossError

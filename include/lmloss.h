@@ -44,6 +44,7 @@ typedef enum {
     LMLOSS_OK = 0,
     LMLOSS_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, ld < V, ...        */
     LMLOSS_ERR_UNSUPPORTED = 2,   /* valid but not served: a launch shape that does not fit, */
+                                  /* a row too long to stage (see lmloss_forward_backward),  */
                                   /* T >= 2^30, a shard call with a teacher or policy term    */
     LMLOSS_ERR_CUDA = 3,          /* a CUDA runtime call failed                            */
     LMLOSS_ERR_BAD_TARGET = 4,    /* device: target not in [0, V) and not -100             */
@@ -164,6 +165,11 @@ lmloss_status lmloss_check_args(const lmloss_args* args);
  *     [Fast-LLM PR 552, "Approach": GSPO's backward follows its eager seam].
  * A teacher combines with every other term, GSPO included (its gradient pass
  * reads the teacher's row statistics back from the workspace).
+ * Row length: a row is staged across at most 16 CTAs, each slice in one CTA's
+ * shared memory (227 KB on GB300), so V is at most 1,835,008 for bf16 logits
+ * (917,504 with a teacher) and half that for fp32; a longer row returns
+ * LMLOSS_ERR_UNSUPPORTED before anything is launched.  Vocabularies beyond that
+ * go through the vocabulary-shard calls below.
  * loss_out is written on every path.  The gradient is
  *   s * (ce_weight (p - onehot) + 2 z_alpha lse p + kl_weight (p^tau - q) / tau)
  *     + c_r (p - onehot)

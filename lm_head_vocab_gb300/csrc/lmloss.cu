@@ -191,6 +191,8 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     P.NT = NT;
     P.nbuf = nbuf;
     P.smem = fused_smem(a->V, C, nbuf, kl, esz, &P.slice, &P.buf_bytes);
+    // a row whose slices do not fit one CTA's shared memory even at 16 CTAs a row
+    if (P.smem > static_cast<size_t>(h->smem_optin)) return LMLOSS_ERR_UNSUPPORTED;
     lmloss_status st = raise_limits(P.fn, h->device, h->smem_optin);
     if (st != LMLOSS_OK) return st;
     cudaLaunchConfig_t cfg{};

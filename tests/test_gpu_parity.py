@@ -237,6 +237,31 @@ def test_gspo_with_teacher(dev, handle, tau):
     assert handle.call_info()["path"] == 2
 
 
+FP32_CASES = [
+    ("gspo_z_bf16", dict(T=512, V=20011, packed_len=128), {}),
+    ("gspo_z_bf16", dict(T=512, V=20011, packed_len=128),
+     dict(teacher_sigma=1.0, kl_weight=0.5, temperature=2.0, ce_weight=0.3)),
+    ("confident_bf16", dict(T=64, V=30001), {}),
+    ("ce_z_kl_bf16", dict(T=48, V=20011), {}),
+]
+
+
+@pytest.mark.parametrize("name,shape,params", FP32_CASES,
+                         ids=["gspo", "gspo_teacher_tau2", "confident", "ce_z_kl"])
+def test_fp32_paths(dev, handle, name, shape, params):
+    """The fp32 instantiations on the paths the bf16 workloads take: GSPO's
+    three passes (with and without a teacher), planted confident rows, and
+    distillation; gradients within 1e-6 absolute, as for ce_fp32_small."""
+    from dataclasses import replace
+    w = replace(workloads.get(name).with_shape(**shape), dtype="fp32", **params)
+    case = Case(w, dev)
+    R, g_ref, scale = oracle.forward_backward(case.P, with_scale=True)
+    _, out = run(handle, case)
+    compare_all(case, out, R, g_ref, f"fp32 {name} {params}", scale)
+    if w.has_gspo:
+        assert np.array_equal(out.seg_count.cpu().numpy(), R.seam.n)
+
+
 def test_launch_config_rejects_unbuilt_shapes(dev, handle):
     """Only the block sizes the library is built for are accepted."""
     from lm_head_vocab_gb300.lmloss import LMLossError

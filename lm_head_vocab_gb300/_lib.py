@@ -16,10 +16,10 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_BUILD, "liblmloss.so")
 HEADER = os.path.join(_ROOT, "include", "lmloss.h")
 # (source, extra flags, object): the host code with the small kernels, and the
-# staged-row kernel's six (dtype, teacher, temperature) instantiation sets, one
-# object each so that they compile in parallel
+# staged-row kernel's eight (dtype, teacher, temperature, entropy) instantiation
+# sets, one object each so that they compile in parallel
 UNITS = [("lmloss.cu", [], "lmloss.o")] + [
-    ("fused_inst.cu", [f"-DLMLOSS_FUSED_VARIANT={k}"], f"fused_{k}.o") for k in range(6)]
+    ("fused_inst.cu", [f"-DLMLOSS_FUSED_VARIANT={k}"], f"fused_{k}.o") for k in range(8)]
 DEPENDS = ["lmloss.cu", "fused_inst.cu", "fused_entry.cuh", "kernels.cuh", "aux_kernels.cuh", "ptx.cuh"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",

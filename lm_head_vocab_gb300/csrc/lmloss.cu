@@ -98,15 +98,19 @@ lmloss_status check(const lmloss_args* a, bool need_loss = true)
 }
 
 // ------------------------------------------------------------ launch plans
-// tau: distillation at a temperature other than 1 (kl only)
-const void* pick_fused(bool bf16, bool kl, bool tau, int nt, bool stats)
+// tau: distillation at a temperature other than 1 (kl only); ent: the entropy
+// output, a compile-time choice without a teacher (with one the kernel decides
+// at run time)
+const void* pick_fused(bool bf16, bool kl, bool tau, bool ent, int nt, bool stats)
 {
-    if (bf16) {
-        if (!kl) return fused_entry<true, false, false>(nt, stats);
-        return tau ? fused_entry<true, true, true>(nt, stats) : fused_entry<true, true, false>(nt, stats);
+    if (!kl) {
+        if (ent) return bf16 ? fused_entry<true, false, false, true>(nt, stats)
+                             : fused_entry<false, false, false, true>(nt, stats);
+        return bf16 ? fused_entry<true, false, false, false>(nt, stats) : fused_entry<false, false, false, false>(nt, stats);
     }
-    if (!kl) return fused_entry<false, false, false>(nt, stats);
-    return tau ? fused_entry<false, true, true>(nt, stats) : fused_entry<false, true, false>(nt, stats);
+    if (bf16)
+        return tau ? fused_entry<true, true, true, false>(nt, stats) : fused_entry<true, true, false, false>(nt, stats);
+    return tau ? fused_entry<false, true, true, false>(nt, stats) : fused_entry<false, true, false, false>(nt, stats);
 }
 
 struct FusedPlan {
@@ -185,7 +189,7 @@ lmloss_status plan_fused(lmloss_ctx* h, const lmloss_args* a, int mode, FusedPla
     }
     if (a->T >= (int64_t(1) << 30)) return LMLOSS_ERR_UNSUPPORTED;   // row indices are 32-bit in the kernel
     if (C < 1 || C > 16 || (nbuf != 1 && nbuf != 2)) return LMLOSS_ERR_UNSUPPORTED;
-    P.fn = pick_fused(bf16, kl, kl && a->temperature != 1.0f, NT, mode == kModeStats);
+    P.fn = pick_fused(bf16, kl, kl && a->temperature != 1.0f, a->entropy_out != nullptr, NT, mode == kModeStats);
     if (!P.fn) return LMLOSS_ERR_UNSUPPORTED;
     P.C = C;
     P.NT = NT;

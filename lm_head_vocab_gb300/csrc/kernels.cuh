@@ -748,19 +748,26 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
         int next_t_pf = -100;
         if (tid == 0 && rank == 0 && claim_row < p.T) next_t_pf = row_target(p, claim_row);
 
-        // GSPO gradient pass: the row's statistics and segment coefficient come
-        // from the workspace; start those loads now, they are needed after the wait
+        // Per-row inputs of the merge: GRPO's advantage and old log-prob, and in
+        // GSPO's gradient pass the row's statistics and segment coefficient from
+        // the workspace.  With a teacher they are loaded here, their latency under
+        // the passes;
+        // without one, where the merge uses them (measured on GB300: the early
+        // loads cost the teacher-free kernel 1.8% even when neither term is in
+        // the call, and saved the teacher kernel as much)
         float g_lse = 0.f, g_nll = 0.f, g_cr = 0.f, g_adv = 0.f, g_old = 0.f;
-        if (p.tok_adv && mode != kModeGrad && warp == 0 && lane == 0 && act && !bad) {
+        auto load_policy = [&]() {
             g_adv = p.tok_adv[r];
             g_old = p.old_logp[r];
-        }
-        if (mode == kModeGrad && warp == 0 && lane == 0 && act && !bad) {
+        };
+        auto load_grad = [&]() {
             g_lse = p.ws.row_lse[r];
             g_nll = p.ws.row_nll[r];
             const int gs = p.seg_ids ? p.seg_ids[r] : -1;
             g_cr = (gs >= 0 && gs < p.num_segments) ? p.ws.seg_coef[gs] : 0.f;
-        }
+        };
+        if (KL && p.tok_adv && mode != kModeGrad && warp == 0 && lane == 0 && act && !bad) load_policy();
+        if (KL && mode == kModeGrad && warp == 0 && lane == 0 && act && !bad) load_grad();
 
         // ---- pass A: maxima (non-target for z, all columns for u), per warp: each
         // warp takes its sums against its own maxima and the warps' partials are
@@ -1018,6 +1025,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             if (bad && rank == 0 && lane == 0 && mode != kModeGrad) set_error(p.ws.err, kErrBadTarget);
             if (act && mode == kModeGrad) {
                 if (lane == 0) {
+                    if (!KL && !bad) load_grad();
                     // s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot)
                     const float nll = bad ? __int_as_float(0x7fc00000) : g_nll;
                     const float lse = bad ? nll : g_lse;
@@ -1140,6 +1148,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     // when the unclipped branch is taken its gradient is s A rho (p - onehot)
                     float c_r = 0.f, pol = 0.f;
                     if (p.tok_adv) {
+                        if (!KL && !bad) load_policy();
                         const float rho = expf(-nll - g_old);
                         const float rc = fminf(fmaxf(rho, 1.f - p.eps_lo), 1.f + p.eps_hi);
                         pol = -fminf(rho * g_adv, rc * g_adv);

@@ -1023,7 +1023,10 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
             const int next_row = __shfl_sync(0xffffffffu, q.next_row, 0);
             const int next_t = __shfl_sync(0xffffffffu, q.next_t, 0);
             if (bad && rank == 0 && lane == 0 && mode != kModeGrad) set_error(p.ws.err, kErrBadTarget);
-            if (act && mode == kModeGrad) {
+            // (the statistics instantiation never runs GSPO's gradient mode, and only
+            // it runs the vocabulary shards' statistics pass: each branch is compiled
+            // where it can be taken)
+            if (!EARLY && act && mode == kModeGrad) {
                 if (lane == 0) {
                     if (!KL && !bad) load_grad();
                     // s (w_ce (p - onehot) + 2 alpha lse p) + c_r (p - onehot)
@@ -1075,7 +1078,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                     if (TAU) St += __shfl_xor_sync(0xffffffffu, St, off);
                 }
                 const float ztf = Zt;
-                if (p.part_out) {
+                if (EARLY && p.part_out) {
                     // vocabulary shard, statistics pass: the shard's partials go out as they
                     // are and are merged across shards by shard_merge_kernel
                     if (lane == 0 && rank == 0) {
@@ -1185,7 +1188,7 @@ __global__ void __launch_bounds__(NT, (fused_min_blocks<KL, NT>())) fused_kernel
                 }
             } else if (lane == 0 && rank == 0 && mode != kModeGrad) {
                 p.ws.row_nll[r] = 0.f; p.ws.row_lse[r] = 0.f; p.ws.row_kl[r] = 0.f; p.ws.row_pol[r] = 0.f;
-                if (p.part_out) {
+                if (EARLY && p.part_out) {
                     float* o = p.part_out + 4 * r;
                     o[0] = -INFINITY; o[1] = 0.f; o[2] = 0.f; o[3] = 0.f;
                 }

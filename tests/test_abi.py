@@ -100,3 +100,13 @@ def test_struct_layout_matches_header():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"(\w+)\s*;", body)
     assert fields == [f for f, _ in L.lmloss_args._fields_]
+
+
+def test_call_info_layout_matches_header():
+    import re
+    txt = open(L.HEADER).read()
+    i = txt.index("} lmloss_call_info;")
+    body = txt[txt.rindex("typedef struct {", 0, i):i]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f for f, _ in L.lmloss_call_info._fields_]

@@ -181,6 +181,32 @@ lmloss_status lmloss_check_args(const lmloss_args* args);
  */
 lmloss_status lmloss_forward_backward(lmloss_handle handle, const lmloss_args* args, cudaStream_t stream);
 
+/*
+ * lmloss_forward_backward for logits that are in host memory: the call copies
+ * them into the device buffer args->logits (and the teacher's into
+ * args->teacher_logits) itself, in chunks of chunk_rows rows (0: T / 8, at
+ * most 64 chunks), on a stream of the handle's own, and launches each chunk's
+ * staged-row kernel on `stream` as soon as that chunk has landed, so the
+ * kernels run under the copies of the chunks after them and the call takes
+ * little more than the copies.
+ *
+ * host_logits (host_teacher) hold the same [T, ld] rows as the device buffer;
+ * host_teacher is non-NULL exactly when args->teacher_logits is.  The copies
+ * overlap only from pinned memory (cudaHostAlloc / cudaHostRegister).  Every
+ * other pointer in args is device memory as for lmloss_forward_backward; the
+ * gradient may be written in place into args->logits.  The copies start after
+ * the work already queued on `stream`; the whole call is complete when `stream`
+ * reaches its end.  Results are bitwise those of lmloss_forward_backward on the
+ * same data (each row's computation does not depend on the chunking, and the
+ * token-mean count and the loss reduction run once over all rows).
+ *
+ * GSPO (segment_ids) is LMLOSS_ERR_UNSUPPORTED: its gradient pass needs every
+ * row's log-prob first.  The first call creates the copy stream and 65 events
+ * (freed by lmloss_destroy); lmloss_set_timing records nothing for this call.
+ */
+lmloss_status lmloss_forward_backward_host(lmloss_handle handle, const lmloss_args* args, const void* host_logits,
+                                           const void* host_teacher, int64_t chunk_rows, cudaStream_t stream);
+
 /* Read and clear the device error word.  Synchronises the handle's device.
  * Returns LMLOSS_OK when no device-side data error occurred since the last read. */
 lmloss_status lmloss_get_device_error(lmloss_handle handle);

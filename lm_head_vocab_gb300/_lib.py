@@ -143,6 +143,8 @@ def load() -> ctypes.CDLL:
         "lmloss_get_device_error": ([h], st),
         "lmloss_status_string": ([st], ctypes.c_char_p),
         "lmloss_set_launch_config": ([h, ctypes.c_int, ctypes.c_int, ctypes.c_int], st),
+        "lmloss_forward_backward_host": ([h, ctypes.POINTER(lmloss_args), ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int64, ctypes.c_void_p], st),
         "lmloss_set_timing": ([h, ctypes.c_int], st),
         "lmloss_get_timing": ([h, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)], st),
         "lmloss_get_call_info": ([h, ctypes.POINTER(lmloss_call_info)], st),
@@ -202,6 +204,11 @@ def lmloss_forward_backward(handle, args: lmloss_args, stream: int) -> int:
 
 def lmloss_get_device_error(handle) -> int:
     return load().lmloss_get_device_error(handle)
+
+
+def lmloss_forward_backward_host(handle, args, host_logits, host_teacher, chunk_rows: int, stream) -> int:
+    return load().lmloss_forward_backward_host(handle, ctypes.byref(args), host_logits, host_teacher, chunk_rows,
+                                               ctypes.c_void_p(stream))
 
 
 def lmloss_set_launch_config(handle, cluster: int = 0, threads: int = 0, nbuf: int = 0) -> int:

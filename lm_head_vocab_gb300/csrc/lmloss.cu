@@ -1,6 +1,7 @@
 // Host side of the lmloss C ABI: argument validation, workspace, launch
 // planning and kernel sequencing.  Every step of the loss runs in the kernels
 // of kernels.cuh; nothing here touches tensor data.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -32,6 +33,13 @@ struct lmloss_ctx {
     lmloss_call_info info{};
     int num_sms = 0;
     int smem_optin = 0;
+    // lmloss_forward_backward_host: a stream of the handle's own for the rows'
+    // copies, and events: [0] the caller's stream reached the call, [1 + k]
+    // chunk k has landed (created on first use)
+    static constexpr int kMaxChunks = 64;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t cev[kMaxChunks + 1] = {};
+    bool copy_ready = false;
 };
 
 namespace {
@@ -265,6 +273,35 @@ void fill_params(const lmloss_ctx* h, const lmloss_args* a, CallParams& p)
     p.part_out = nullptr;
 }
 
+// The parameters of rows [r0, r1) as a call of their own: every row-indexed
+// pointer (inputs, per-row outputs and the workspace's per-row results) moved
+// to row r0, so each row keeps its place; the token scale still comes from the
+// whole call's count.
+CallParams chunk_params(const CallParams& p, const lmloss_args* a, int64_t r0, int64_t r1)
+{
+    CallParams c = p;
+    const size_t off = static_cast<size_t>(r0) * static_cast<size_t>(a->ld) * (a->dtype == LMLOSS_BF16 ? 2u : 4u);
+    c.logits = static_cast<const unsigned char*>(p.logits) + off;
+    if (p.teacher) c.teacher = static_cast<const unsigned char*>(p.teacher) + off;
+    if (p.grad) c.grad = static_cast<unsigned char*>(p.grad) + off;
+    c.targets = p.targets + r0;
+    if (p.mask) c.mask = p.mask + r0;
+    c.T = r1 - r0;
+    if (p.logp_out) c.logp_out = p.logp_out + r0;
+    if (p.lse_out) c.lse_out = p.lse_out + r0;
+    if (p.kl_out) c.kl_out = p.kl_out + r0;
+    if (p.entropy_out) c.entropy_out = p.entropy_out + r0;
+    if (p.tok_adv) c.tok_adv = p.tok_adv + r0;
+    if (p.old_logp) c.old_logp = p.old_logp + r0;
+    c.ws.row_nll = p.ws.row_nll + r0;
+    c.ws.row_lse = p.ws.row_lse + r0;
+    c.ws.row_kl = p.ws.row_kl + r0;
+    c.ws.row_pol = p.ws.row_pol + r0;
+    c.ws.row_tu = p.ws.row_tu + 2 * r0;
+    c.ws.row_tt = p.ws.row_tt + 4 * r0;
+    return c;
+}
+
 lmloss_status launch_err()
 {
     return cudaGetLastError() == cudaSuccess ? LMLOSS_OK : LMLOSS_ERR_CUDA;
@@ -420,6 +457,10 @@ lmloss_status lmloss_destroy(lmloss_handle h)
     if (!h) return LMLOSS_ERR_INVALID_ARG;
     DeviceGuard g(h->device);
     cudaDeviceSynchronize();
+    if (h->copy_ready) {
+        cudaStreamDestroy(h->copy_stream);
+        for (cudaEvent_t e : h->cev) cudaEventDestroy(e);
+    }
     for (int i = 0; i < 2 * h->ev_created; ++i) cudaEventDestroy(h->ev[i]);
     std::free(h->ev);
     cudaError_t e = cudaFree(h->ws_mem);
@@ -565,6 +606,99 @@ lmloss_status lmloss_forward_backward(lmloss_handle h, const lmloss_args* a, cud
     if (ev_slot >= 0) {
         cudaEventRecord(h->ev[2 * ev_slot + 1], stream);
         h->ev_used = ev_slot + 1;
+    }
+    if ((st = launch_reduce(p, red_blocks, stream)) != LMLOSS_OK) return st;
+    info.launches += 1;
+    h->info = info;
+    return LMLOSS_OK;
+}
+
+lmloss_status lmloss_forward_backward_host(lmloss_handle h, const lmloss_args* a, const void* host_logits,
+                                           const void* host_teacher, int64_t chunk_rows, cudaStream_t stream)
+{
+    if (!h) return LMLOSS_ERR_INVALID_ARG;
+    lmloss_status st = check(a);
+    if (st != LMLOSS_OK) return st;
+    if (a->T > h->max_T || chunk_rows < 0) return LMLOSS_ERR_INVALID_ARG;
+    if (a->T > 0 && !host_logits) return LMLOSS_ERR_INVALID_ARG;
+    if ((host_teacher != nullptr) != (a->teacher_logits != nullptr)) return LMLOSS_ERR_INVALID_ARG;
+    // GSPO's gradient pass needs every row's log-prob first: no row can start early
+    if (a->segment_ids) return LMLOSS_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    if (!g.ok) return LMLOSS_ERR_CUDA;
+    if (!h->copy_ready) {
+        // all or nothing: what was created is destroyed again if any creation fails
+        cudaStream_t cs = nullptr;
+        cudaEvent_t ev[lmloss_ctx::kMaxChunks + 1] = {};
+        int made = 0;
+        bool ok = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) == cudaSuccess;
+        for (; ok && made < lmloss_ctx::kMaxChunks + 1; ++made)
+            ok = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (int i = 0; i < made; ++i)
+                if (ev[i]) cudaEventDestroy(ev[i]);
+            if (cs) cudaStreamDestroy(cs);
+            cudaGetLastError();
+            return LMLOSS_ERR_CUDA;
+        }
+        h->copy_stream = cs;
+        for (int i = 0; i <= lmloss_ctx::kMaxChunks; ++i) h->cev[i] = ev[i];
+        h->copy_ready = true;
+    }
+
+    CallParams p{};
+    fill_params(h, a, p);
+    lmloss_call_info info{};
+    int64_t rb = (a->T + 63) / 64;
+    if (rb > kRedBlocks) rb = kRedBlocks;
+    const int red_blocks = rb < 1 ? 1 : static_cast<int>(rb);
+    // the token mean's count over every row, before any chunk's gradient
+    if (a->reduction == LMLOSS_REDUCE_TOKEN_MEAN) {
+        count_kernel<<<red_blocks, 256, 0, stream>>>(p);
+        if ((st = launch_err()) != LMLOSS_OK) return st;
+        info.launches = 1;
+    }
+    const int64_t T = a->T;
+    if (T > 0) {
+        // chunks: 8 by default, at most kMaxChunks
+        int64_t rows = chunk_rows > 0 ? chunk_rows : (T + 7) / 8;
+        if ((T + rows - 1) / rows > lmloss_ctx::kMaxChunks) rows = (T + lmloss_ctx::kMaxChunks - 1) / lmloss_ctx::kMaxChunks;
+        const int64_t nchunks = (T + rows - 1) / rows;
+        const size_t esz = a->dtype == LMLOSS_BF16 ? 2u : 4u;
+        const size_t row_bytes = static_cast<size_t>(a->ld) * esz;
+        // the copies wait for the caller's earlier work on its stream (which may
+        // still read or write these buffers), then go out back to back
+        if (cudaEventRecord(h->cev[0], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(h->copy_stream, h->cev[0], 0) != cudaSuccess)
+            return LMLOSS_ERR_CUDA;
+        for (int64_t k = 0; k < nchunks; ++k) {
+            const int64_t r0 = k * rows, r1 = std::min(T, r0 + rows);
+            // rows r0 .. r1 - 1: every column of the full rows, the last row's V
+            const size_t off = static_cast<size_t>(r0) * row_bytes;
+            const size_t bytes = static_cast<size_t>(r1 - r0 - 1) * row_bytes + static_cast<size_t>(a->V) * esz;
+            if (cudaMemcpyAsync(static_cast<unsigned char*>(const_cast<void*>(a->logits)) + off,
+                                static_cast<const unsigned char*>(host_logits) + off, bytes, cudaMemcpyHostToDevice,
+                                h->copy_stream) != cudaSuccess)
+                return LMLOSS_ERR_CUDA;
+            if (host_teacher &&
+                cudaMemcpyAsync(static_cast<unsigned char*>(const_cast<void*>(a->teacher_logits)) + off,
+                                static_cast<const unsigned char*>(host_teacher) + off, bytes, cudaMemcpyHostToDevice,
+                                h->copy_stream) != cudaSuccess)
+                return LMLOSS_ERR_CUDA;
+            if (cudaEventRecord(h->cev[1 + k], h->copy_stream) != cudaSuccess) return LMLOSS_ERR_CUDA;
+        }
+        // each chunk's staged-row kernel as soon as its rows have landed: the
+        // kernels run under the copies of the chunks after them
+        const int mode = a->grad_out ? kModeFused : kModeStats;
+        for (int64_t k = 0; k < nchunks; ++k) {
+            const int64_t r0 = k * rows, r1 = std::min(T, r0 + rows);
+            if (cudaStreamWaitEvent(stream, h->cev[1 + k], 0) != cudaSuccess) return LMLOSS_ERR_CUDA;
+            lmloss_args ac = *a;
+            ac.T = r1 - r0;
+            CallParams pc = chunk_params(p, a, r0, r1);
+            if ((st = launch_fused(h, &ac, pc, mode, stream, info)) != LMLOSS_OK) return st;
+        }
+        info.path = a->grad_out ? 0 : 1;
     }
     if ((st = launch_reduce(p, red_blocks, stream)) != LMLOSS_OK) return st;
     info.launches += 1;

@@ -203,6 +203,32 @@ class LMLoss:
         self.call(args, stream)
         return out
 
+    def call_host(self, args: "_lib.lmloss_args", host_logits: torch.Tensor, host_teacher=None,
+                  chunk_rows: int = 0, stream: Optional[torch.cuda.Stream] = None):
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        st = _lib.lmloss_forward_backward_host(self.handle, args, _ptr(host_logits), _ptr(host_teacher),
+                                               int(chunk_rows), s.cuda_stream)
+        if st != _lib.LMLOSS_OK:
+            raise LMLossError(st, "lmloss_forward_backward_host")
+
+    def forward_backward_host(self, host_logits: torch.Tensor, logits: torch.Tensor, targets: torch.Tensor,
+                              loss_mask=None, *, host_teacher=None, chunk_rows: int = 0,
+                              stream: Optional[torch.cuda.Stream] = None, **kw) -> Outputs:
+        """forward_backward with the logits (and the teacher's) taken from host
+        tensors: the library copies them into `logits` (and `teacher_logits`) in
+        row chunks and runs each chunk's kernel as soon as it has landed.  The
+        host tensors must match the device ones in dtype, shape and strides, and
+        should be pinned."""
+        for hst, d, name in ((host_logits, logits, "host_logits"), (host_teacher, kw.get("teacher_logits"), "host_teacher")):
+            if (hst is None) != (d is None):
+                raise ValueError(f"{name} and its device tensor go together")
+            if hst is not None and (hst.device.type != "cpu" or hst.dtype != d.dtype or hst.shape != d.shape
+                                    or hst.stride() != d.stride()):
+                raise ValueError(f"{name} must be a host tensor matching its device tensor")
+        args, out, _keep = self.build_args(logits, targets, loss_mask, **kw)
+        self.call_host(args, host_logits, host_teacher, chunk_rows, stream)
+        return out
+
     # ------------------------------------------- vocabulary-split rows
     def _stream(self, stream):
         return (torch.cuda.current_stream(self.device) if stream is None else stream).cuda_stream

@@ -21,8 +21,8 @@ Output: one JSON line on rank 0.
   e2e        the same metric through the C ABI with host buffers: each step
              takes the step's inputs from pinned host memory (the logits through
              lmloss_forward_backward_host, which copies them in row chunks and
-             runs each chunk's kernel as it lands; GSPO, which it does not take,
-             copies them first and then calls) and reads the 5 loss values back
+             runs each chunk's kernel as it lands) and reads the 5 loss values
+             back
   roofline   the staged-row kernel's algorithmic bytes (reads of active rows,
              the gradient write, side inputs) / its CUDA-event duration (events
              around each launch, in a second pass of K steps so that they do not
@@ -484,26 +484,16 @@ def time_workload(args, name, dev, world, rank, main: bool):
                   (gkw["old_logprobs"], gkw["old_logprobs"].cpu().pin_memory())]
             h2d += sum(hs.numel() * hs.element_size() for _, hs in hg)
 
-        # the logits (and the teacher's) through the host entry point, which copies
-        # them itself; GSPO needs every row before any gradient, so there the
-        # copies come first and the regular call after them
-        via_host = prob.gspo is None
-
+        # the small inputs by torch copies, the logits (and the teacher's) by the
+        # host entry point, which copies them itself in row chunks
         def e2e_step():
-            if not via_host:
-                prob.logits.copy_(prob.hx, non_blocking=True)
-                if prob.hu is not None:
-                    prob.teacher.copy_(prob.hu, non_blocking=True)
             tg.copy_(ht, non_blocking=True)
             if hm is not None:
                 mk.copy_(hm, non_blocking=True)
             if hg is not None:
                 for dst, src in hg:
                     dst.copy_(src, non_blocking=True)
-            if via_host:
-                h.call_host(a, prob.hx, prob.hu, 0, stream)
-            else:
-                h.call(a, stream)
+            h.call_host(a, prob.hx, prob.hu, 0, stream)
             hloss.copy_(out.loss, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):

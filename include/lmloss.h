@@ -200,9 +200,10 @@ lmloss_status lmloss_forward_backward(lmloss_handle handle, const lmloss_args* a
  * same data (each row's computation does not depend on the chunking, and the
  * token-mean count and the loss reduction run once over all rows).
  *
- * GSPO (segment_ids) is LMLOSS_ERR_UNSUPPORTED: its gradient pass needs every
- * row's log-prob first.  The first call creates the copy stream and 65 events
- * (freed by lmloss_destroy); lmloss_set_timing records nothing for this call.
+ * With GSPO (segment_ids) the chunks run the statistics pass; the segment step
+ * and the gradient pass, which need every row's log-prob, follow once all rows
+ * are in.  The first call creates the copy stream and 65 events (freed by
+ * lmloss_destroy); lmloss_set_timing records nothing for this call.
  */
 lmloss_status lmloss_forward_backward_host(lmloss_handle handle, const lmloss_args* args, const void* host_logits,
                                            const void* host_teacher, int64_t chunk_rows, cudaStream_t stream);

@@ -293,6 +293,7 @@ CallParams chunk_params(const CallParams& p, const lmloss_args* a, int64_t r0, i
     if (p.entropy_out) c.entropy_out = p.entropy_out + r0;
     if (p.tok_adv) c.tok_adv = p.tok_adv + r0;
     if (p.old_logp) c.old_logp = p.old_logp + r0;
+    if (p.seg_ids) c.seg_ids = p.seg_ids + r0;
     c.ws.row_nll = p.ws.row_nll + r0;
     c.ws.row_lse = p.ws.row_lse + r0;
     c.ws.row_kl = p.ws.row_kl + r0;
@@ -622,8 +623,8 @@ lmloss_status lmloss_forward_backward_host(lmloss_handle h, const lmloss_args* a
     if (a->T > h->max_T || chunk_rows < 0) return LMLOSS_ERR_INVALID_ARG;
     if (a->T > 0 && !host_logits) return LMLOSS_ERR_INVALID_ARG;
     if ((host_teacher != nullptr) != (a->teacher_logits != nullptr)) return LMLOSS_ERR_INVALID_ARG;
-    // GSPO's gradient pass needs every row's log-prob first: no row can start early
-    if (a->segment_ids) return LMLOSS_ERR_UNSUPPORTED;
+    if (a->segment_ids && a->num_segments > h->max_S) return LMLOSS_ERR_INVALID_ARG;
+    const bool gspo = a->segment_ids != nullptr;
     DeviceGuard g(h->device);
     if (!g.ok) return LMLOSS_ERR_CUDA;
     if (!h->copy_ready) {
@@ -652,8 +653,9 @@ lmloss_status lmloss_forward_backward_host(lmloss_handle h, const lmloss_args* a
     int64_t rb = (a->T + 63) / 64;
     if (rb > kRedBlocks) rb = kRedBlocks;
     const int red_blocks = rb < 1 ? 1 : static_cast<int>(rb);
-    // the token mean's count over every row, before any chunk's gradient
-    if (a->reduction == LMLOSS_REDUCE_TOKEN_MEAN) {
+    // the token mean's count over every row, before any chunk's gradient (it also
+    // clears GSPO's segment accumulators)
+    if (gspo || a->reduction == LMLOSS_REDUCE_TOKEN_MEAN) {
         count_kernel<<<red_blocks, 256, 0, stream>>>(p);
         if ((st = launch_err()) != LMLOSS_OK) return st;
         info.launches = 1;
@@ -688,8 +690,10 @@ lmloss_status lmloss_forward_backward_host(lmloss_handle h, const lmloss_args* a
             if (cudaEventRecord(h->cev[1 + k], h->copy_stream) != cudaSuccess) return LMLOSS_ERR_CUDA;
         }
         // each chunk's staged-row kernel as soon as its rows have landed: the
-        // kernels run under the copies of the chunks after them
-        const int mode = a->grad_out ? kModeFused : kModeStats;
+        // kernels run under the copies of the chunks after them.  With GSPO that
+        // is the statistics pass; the seam and the gradient pass follow once
+        // every row is in, as in the regular call.
+        const int mode = (a->grad_out && !gspo) ? kModeFused : kModeStats;
         for (int64_t k = 0; k < nchunks; ++k) {
             const int64_t r0 = k * rows, r1 = std::min(T, r0 + rows);
             if (cudaStreamWaitEvent(stream, h->cev[1 + k], 0) != cudaSuccess) return LMLOSS_ERR_CUDA;
@@ -698,7 +702,18 @@ lmloss_status lmloss_forward_backward_host(lmloss_handle h, const lmloss_args* a
             CallParams pc = chunk_params(p, a, r0, r1);
             if ((st = launch_fused(h, &ac, pc, mode, stream, info)) != LMLOSS_OK) return st;
         }
-        info.path = a->grad_out ? 0 : 1;
+        info.path = gspo ? 2 : (a->grad_out ? 0 : 1);
+        if (gspo) {
+            const int tg = 256;
+            int64_t gb = (T + tg - 1) / tg;
+            if (gb > 4LL * h->num_sms) gb = 4LL * h->num_sms;
+            seam_accum_kernel<<<static_cast<unsigned>(gb), tg, 0, stream>>>(p);
+            if ((st = launch_err()) != LMLOSS_OK) return st;
+            seam_finish_kernel<<<1, 1024, 0, stream>>>(p);
+            if ((st = launch_err()) != LMLOSS_OK) return st;
+            info.launches += 2;
+            if (a->grad_out && (st = launch_fused(h, a, p, kModeGrad, stream, info)) != LMLOSS_OK) return st;
+        }
     }
     if ((st = launch_reduce(p, red_blocks, stream)) != LMLOSS_OK) return st;
     info.launches += 1;

@@ -3,9 +3,9 @@ chunks on a stream of the handle's own and starts each chunk's kernel as soon
 as it has landed.  Every output must be the bits of lmloss_forward_backward on
 the same data (a row's computation does not depend on the chunking; the token
 count and the loss reduction run once over all rows), for several chunkings,
-both reductions, forward only, a teacher, GRPO's per-token inputs, the entropy
-and padded rows; and the copies must follow the caller's earlier work on its
-stream."""
+both reductions, forward only, a teacher, GRPO's per-token inputs, GSPO, the
+entropy and padded rows; and the copies must follow the caller's earlier work on
+its stream."""
 from dataclasses import replace
 
 import numpy as np
@@ -32,7 +32,7 @@ def dev():
 @pytest.fixture(scope="module")
 def handle(dev):
     from lm_head_vocab_gb300 import LMLoss
-    h = LMLoss(0, max_T=4096, max_segments=1)
+    h = LMLoss(0, max_T=4096, max_segments=4096)
     yield h
     h.close()
 
@@ -158,18 +158,40 @@ def test_copies_follow_earlier_work_on_the_stream(dev, handle):
     assert np.array_equal(_bits(d_x[:, :w.V]), _bits(ref.grad[:, :w.V]))
 
 
-def test_rejects_gspo_and_unpaired_teacher(dev, handle):
-    from lm_head_vocab_gb300 import _lib
-    from lm_head_vocab_gb300.lmloss import LMLossError
-    w = workloads.get("gspo_z_bf16").with_shape(T=256, V=4096, packed_len=64)
+@pytest.mark.parametrize("teacher", [False, True], ids=["gspo", "gspo_teacher"])
+def test_gspo(dev, handle, teacher):
+    """GSPO: the chunks run the statistics pass as they land; the seam and the
+    gradient pass follow over all rows.  Same bits as the device call."""
+    w = workloads.get("gspo_z_bf16").with_shape(T=1024, V=20011, packed_len=256)
+    if teacher:
+        w = replace(w, teacher_sigma=1.0, kl_weight=0.5, temperature=2.0, ce_weight=0.3)
+    case = Case(w, dev)
+    inp = case.device_inputs()
+    kw = case.kwargs()
+    g = dict(segment_ids=inp["segment_ids"], advantages=inp["advantages"], old_logprobs=inp["old_logprobs"])
+    want = WANT + ("seg",)
+    ref = handle.forward_backward(inp["logits"], inp["targets"], inp["loss_mask"],
+                                  teacher_logits=inp["teacher_logits"], grad="new", want=want, **g, **kw)
+    torch.cuda.synchronize()
+    hx = inp["logits"].cpu().pin_memory()
+    hu = None if inp["teacher_logits"] is None else inp["teacher_logits"].cpu().pin_memory()
+    d_u = None if hu is None else torch.empty_like(inp["teacher_logits"])
+    out = handle.forward_backward_host(hx, torch.empty_like(inp["logits"]), inp["targets"], inp["loss_mask"],
+                                       host_teacher=hu, teacher_logits=d_u, chunk_rows=100, grad="new",
+                                       want=want, **g, **kw)
+    torch.cuda.synchronize()
+    assert handle.device_error() == 0
+    assert handle.call_info()["path"] == 2
+    _same(out, ref, "gspo", w.V)
+    for k in ("seg_count", "seg_ratio", "seg_flag", "seg_loss"):
+        assert torch.equal(getattr(out, k), getattr(ref, k)), k
+
+
+def test_rejects_unpaired_host_teacher(dev, handle):
+    w = workloads.get("ce_z_bf16").with_shape(T=64, V=4096)
     case = Case(w, dev)
     inp = case.device_inputs()
     hx = inp["logits"].cpu().pin_memory()
-    with pytest.raises(LMLossError) as e:
-        handle.forward_backward_host(hx, torch.empty_like(inp["logits"]), inp["targets"], inp["loss_mask"],
-                                     segment_ids=inp["segment_ids"], advantages=inp["advantages"],
-                                     old_logprobs=inp["old_logprobs"], grad="new", **case.kwargs())
-    assert e.value.status == _lib.LMLOSS_ERR_UNSUPPORTED
     with pytest.raises(ValueError):
         handle.forward_backward_host(hx, torch.empty_like(inp["logits"]), inp["targets"], host_teacher=hx,
                                      grad="new")

@@ -2,12 +2,15 @@
  * Using the lmloss C ABI from C, with no Python: one loss and gradient call on
  * a batch read from files.
  *
- *   lmloss_c_example T V logits.f32 targets.i64 grad_out.f32
+ *   lmloss_c_example T V logits.f32 targets.i64 grad_out.f32 [host]
  *
  * logits.f32 holds T*V float32 values (row-major), targets.i64 T int64 targets
  * (-100 ignores a row).  The gradient of the token-mean loss is written to
  * grad_out.f32 (T*V float32), and the five losses (total, cross-entropy,
  * z-loss, KL, policy) are printed on one line.  The z-loss weight is 1e-4.
+ * With "host" the logits stay in host memory (registered as pinned) and
+ * lmloss_forward_backward_host copies them itself, in row chunks under the
+ * chunks' kernels; the results are the same bits.
  *
  * Build (from the repository root, after the library is built):
  *   cc -std=c11 -Iinclude -I/usr/local/cuda/include examples/lmloss_c_example.c \
@@ -60,10 +63,11 @@ static int write_file(const char* path, const void* buf, size_t bytes)
 
 int main(int argc, char** argv)
 {
-    if (argc != 6) {
-        fprintf(stderr, "usage: %s T V logits.f32 targets.i64 grad_out.f32\n", argv[0]);
+    if (argc != 6 && !(argc == 7 && strcmp(argv[6], "host") == 0)) {
+        fprintf(stderr, "usage: %s T V logits.f32 targets.i64 grad_out.f32 [host]\n", argv[0]);
         return 2;
     }
+    const int from_host = argc == 7;
     const int64_t T = atoll(argv[1]), V = atoll(argv[2]);
     if (T < 1 || V < 1) {
         fprintf(stderr, "T and V must be positive\n");
@@ -85,7 +89,10 @@ int main(int argc, char** argv)
     CHECK_CUDA(cudaMalloc((void**)&d_g, n * sizeof(float)));
     CHECK_CUDA(cudaMalloc((void**)&d_t, (size_t)T * sizeof(int64_t)));
     CHECK_CUDA(cudaMalloc((void**)&d_loss, 5 * sizeof(float)));
-    CHECK_CUDA(cudaMemcpy(d_x, x, n * sizeof(float), cudaMemcpyHostToDevice));
+    if (from_host)
+        CHECK_CUDA(cudaHostRegister(x, n * sizeof(float), cudaHostRegisterDefault));
+    else
+        CHECK_CUDA(cudaMemcpy(d_x, x, n * sizeof(float), cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(d_t, t, (size_t)T * sizeof(int64_t), cudaMemcpyHostToDevice));
 
     lmloss_handle h = NULL;
@@ -107,7 +114,10 @@ int main(int argc, char** argv)
     a.grad_out = d_g;
     a.loss_out = d_loss;
     CHECK_LMLOSS(lmloss_check_args(&a));
-    CHECK_LMLOSS(lmloss_forward_backward(h, &a, 0));   /* the default stream */
+    if (from_host)   /* d_x receives the logits from x, chunk by chunk */
+        CHECK_LMLOSS(lmloss_forward_backward_host(h, &a, x, NULL, 0, 0));
+    else
+        CHECK_LMLOSS(lmloss_forward_backward(h, &a, 0));   /* the default stream */
     CHECK_CUDA(cudaStreamSynchronize(0));
     CHECK_LMLOSS(lmloss_get_device_error(h));
 
@@ -121,6 +131,7 @@ int main(int argc, char** argv)
     printf("%.9g %.9g %.9g %.9g %.9g\n", loss[0], loss[1], loss[2], loss[3], loss[4]);
 
     CHECK_LMLOSS(lmloss_destroy(h));
+    if (from_host) CHECK_CUDA(cudaHostUnregister(x));
     cudaFree(d_x);
     cudaFree(d_g);
     cudaFree(d_t);

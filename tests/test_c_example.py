@@ -59,3 +59,9 @@ def test_c_example_matches_oracle(tmp_path):
     assert loss[3] == 0.0 and loss[4] == 0.0
     assert np.max(np.abs(g - g_ref)) <= 1e-6
     assert np.all(g[[3, 17]] == 0.0)
+    # the logits left in host memory: lmloss_forward_backward_host, same bits
+    r2 = subprocess.run([exe, str(T), str(V), str(tmp_path / "x.f32"), str(tmp_path / "t.i64"),
+                         str(tmp_path / "g2.f32"), "host"], capture_output=True, text=True)
+    assert r2.returncode == 0, r2.stderr
+    assert r2.stdout == r.stdout
+    assert (tmp_path / "g2.f32").read_bytes() == (tmp_path / "g.f32").read_bytes()

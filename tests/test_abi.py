@@ -90,6 +90,8 @@ def test_null_args_and_handle(lib):
     assert lib.lmloss_destroy(None) == L.LMLOSS_ERR_INVALID_ARG
     assert lib.lmloss_get_device_error(None) == L.LMLOSS_ERR_INVALID_ARG
     assert lib.lmloss_set_launch_config(None, 0, 0, 0) == L.LMLOSS_ERR_INVALID_ARG
+    assert lib.lmloss_forward_backward_host(None, ctypes.byref(_args()), None, None, 0, None) == \
+        L.LMLOSS_ERR_INVALID_ARG
 
 
 def test_struct_layout_matches_header():

@@ -203,7 +203,10 @@ lmloss_status lmloss_forward_backward(lmloss_handle handle, const lmloss_args* a
  * With GSPO (segment_ids) the chunks run the statistics pass; the segment step
  * and the gradient pass, which need every row's log-prob, follow once all rows
  * are in.  The first call creates the copy stream and 65 events (freed by
- * lmloss_destroy); lmloss_set_timing records nothing for this call.
+ * lmloss_destroy), so it belongs before any stream capture; later calls can be
+ * captured in a CUDA graph (the copy stream joins the capture through the
+ * events, and a replay copies whatever the host buffers hold then).
+ * lmloss_set_timing records nothing for this call.
  */
 lmloss_status lmloss_forward_backward_host(lmloss_handle handle, const lmloss_args* args, const void* host_logits,
                                            const void* host_teacher, int64_t chunk_rows, cudaStream_t stream);

@@ -215,3 +215,42 @@ def test_padded_rows(dev, handle):
     torch.cuda.synchronize()
     assert handle.device_error() == 0
     _same(out, ref, "padded rows", V)
+
+
+def test_cuda_graph_capture_and_replay(dev, handle):
+    """The host-buffer call captured in a CUDA graph (its copy stream joins the
+    capture through the events) and replayed after new values are written into
+    the pinned host buffer: each replay gives the bits of a direct device call
+    on those values."""
+    w = workloads.get("ce_z_bf16").with_shape(T=512, V=32000)
+    case = Case(w, dev)
+    inp = case.device_inputs()
+    kw = case.kwargs()
+    want = ("logp", "lse", "count")
+    hx = inp["logits"].cpu().pin_memory()
+    x = torch.empty_like(inp["logits"])
+
+    def call():
+        return handle.forward_backward_host(hx, x, inp["targets"], inp["loss_mask"], chunk_rows=100, grad="new",
+                                            want=want, **kw)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()                                   # creates the copy stream and events, outside the capture
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = call()
+    gen = torch.Generator().manual_seed(3)
+    for k in range(3):
+        hx.copy_((inp["logits"].float().cpu() + torch.randn(hx.shape, generator=gen)).to(hx.dtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        direct = handle.forward_backward(hx.to(dev), inp["targets"], inp["loss_mask"], grad="new", want=want, **kw)
+        torch.cuda.synchronize()
+        assert handle.device_error() == 0
+        assert torch.equal(captured.loss, direct.loss), k
+        assert torch.equal(captured.logp, direct.logp) and torch.equal(captured.lse, direct.lse), k
+        assert torch.equal(captured.grad.view(torch.int16), direct.grad.view(torch.int16)), k
